@@ -1,0 +1,238 @@
+"""CPU oracle for the paged KV-cache decode path.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its ``cpu_baseline`` leg and its ``--impl reference`` arm) may
+import or run anything in this package.  The product library never calls it
+and shares no code, header, table or helper with it.
+
+Plain, single-threaded NumPy in float64.  Every function cites the passage of
+the source pages that defines it.  The pages are four web articles on
+PagedAttention / vLLM, cited by title and section:
+
+* P1 "vLLM核心概念：PagedAttention原理、KV Cache分页管理、连续批处理、投机解码概览"
+* P2 "LLM 推理引擎内部原理：PagedAttention、Continuous Batching 与现代推理架构剖析"
+* P3 "LLM 推理优化深度实战：从 PagedAttention 到 Speculative Decoding 的工程架构"
+* P4 the tbr8.org PagedAttention article (its title is not in the extract; cited
+  by host and section heading)
+
+Readings taken where the pages are silent or garbled (each is pinned by a
+test in ``tests/test_oracle_pins.py``):
+
+* query head h reads KV head ``h // (num_heads // num_kv_heads)`` (contiguous
+  GQA grouping; P4 §2.2 gives only the shapes);
+* the softmax runs over all positions t < seq_len of the sequence (P4 §2.2's
+  pseudocode applies it to one scalar score, which is garbled; P2 §2.4 says
+  the softmax and the V weighting follow the scores);
+* the block table is indexed by the logical block index (P2 §2.4's listing
+  indexes it by its length, a typo);
+* a slot < 0 in ``slot_mapping`` writes nothing; seq_len = 0 gives zeros;
+* ``seq_lens`` count the token appended in the same step.
+
+Parity unpinned: P3 §一's "≈512MB" KV-size example; its own formula with its
+stated L=80, d=8192, n=2048 gives 5 GiB, and no head count reproduces 512 MB,
+so no test can pin it.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F16 = "f16"
+BF16 = "bf16"
+
+
+# --------------------------------------------------------------------------
+# element decoding
+# --------------------------------------------------------------------------
+def decode_bits(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """fp16 / bf16 bit patterns (uint16) -> float64, exactly."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == F16:
+        return bits.view(np.float16).astype(np.float64)
+    if dtype == BF16:
+        return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+# --------------------------------------------------------------------------
+# sizes (P4 §一 formula; P2 §1.1 and §4.1 worked numbers)
+# --------------------------------------------------------------------------
+def kv_cache_bytes(num_layers: int, seq_len: int, num_kv_heads: int, head_dim: int,
+                   dtype_size: int = 2) -> int:
+    """Bytes of K plus V for ``seq_len`` tokens: 2 * L * S * H_kv * d * bytes.
+
+    P4 §一 (``kv_cache_size``).  P2 §1.1 writes the same product with D for
+    one head's width.
+    """
+    return 2 * num_layers * seq_len * num_kv_heads * head_dim * dtype_size
+
+
+def num_logical_blocks(num_tokens: int, block_size: int) -> int:
+    """Blocks a sequence of ``num_tokens`` occupies: ceil(num_tokens / block_size).
+
+    P3 §2.1 (``BlockTable.num_blocks``); P4 §3 (``allocate``: 50 tokens -> 4
+    blocks of 16, 4096 -> 256).
+    """
+    return (num_tokens + block_size - 1) // block_size
+
+
+# --------------------------------------------------------------------------
+# slot arithmetic (P2 §2.3 BlockEngine.append_slot; P4 §2.1 three-level map)
+# --------------------------------------------------------------------------
+def slot_for_position(block_table_row, pos: int, block_size: int) -> int:
+    """Flat slot of logical position ``pos``: physical_block * block_size + offset.
+
+    P2 §2.3: a token that lands in the last block at ``len % block_size`` gets
+    ``blocks[-1] * block_size + len % block_size``; P4 §2.1: token t lives in
+    logical block t // block_size, mapped through the table.
+    """
+    return int(block_table_row[pos // block_size]) * block_size + pos % block_size
+
+
+def physical_location(slot: int, block_size: int):
+    """(physical block, offset in block) of a flat slot."""
+    return slot // block_size, slot % block_size
+
+
+# --------------------------------------------------------------------------
+# cache writes (bitwise; operate on uint16 bit arrays in place)
+# --------------------------------------------------------------------------
+def append_ref(key_cache: np.ndarray, value_cache: np.ndarray, k: np.ndarray, v: np.ndarray,
+               slot_mapping: np.ndarray) -> None:
+    """Write each new token's K/V rows into its slot.
+
+    Caches are [num_blocks, block_size, num_kv_heads, head_dim]; k, v are
+    [T, num_kv_heads, head_dim].  For token t with slot >= 0:
+    cache[slot // bs, slot % bs, :, :] = k[t] (P2 §2.3 slot, P1 §4.2.2 "增长").
+    A negative slot writes nothing.
+    """
+    bs = key_cache.shape[1]
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        b, o = physical_location(int(slot), bs)
+        key_cache[b, o] = k[t]
+        value_cache[b, o] = v[t]
+
+
+def copy_blocks_ref(key_caches, value_caches, pairs) -> None:
+    """Copy-on-write block copy: for each (src, dst), cache[dst] = cache[src], every layer.
+
+    P2 §3.1 (``blocks_to_copy`` of the scheduler output, "用于 Copy-on-Write")
+    and §3.3; P1 §4.2.2 ("复制该块后再写入"); P4 §五.  Pairs are applied in order.
+    """
+    for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist():
+        for kc, vc in zip(key_caches, value_caches):
+            kc[dst] = kc[src]
+            vc[dst] = vc[src]
+
+
+# --------------------------------------------------------------------------
+# attention (P4 §2.2 paged_attention_kernel, read per the module docstring)
+# --------------------------------------------------------------------------
+def gather_sequence(cache: np.ndarray, block_table_row, seq_len: int, kv_head: int,
+                    dtype: str) -> np.ndarray:
+    """Contiguous float64 [seq_len, head_dim] rows of one KV head of one sequence.
+
+    Logical block j is physical block table[j]; within it token offset o is
+    position j * block_size + o; positions >= seq_len are never read (P4 §2.2:
+    the loop breaks at seq_len; the last block is partly filled).
+    """
+    bs = cache.shape[1]
+    pieces = []
+    for j in range(num_logical_blocks(seq_len, bs)):
+        b = int(block_table_row[j])
+        n = min(bs, seq_len - j * bs)          # the last block is filled up to seq_len
+        pieces.append(cache[b, :n, kv_head])
+    if not pieces:
+        return np.zeros((0, cache.shape[3]), dtype=np.float64)
+    return decode_bits(np.concatenate(pieces, axis=0), dtype)
+
+
+def softmax_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """Textbook single-query attention: softmax_t(scale * q.K_t) weighted sum of V_t.
+
+    z_t = scale * <q, K_t>;  p_t = exp(z_t - max z);  out = sum_t p_t V_t / sum_t p_t.
+    P4 §2.2 (score = dot(q, k) / sqrt(head_dim), weighted by V); subtracting the
+    maximum leaves the result unchanged and keeps exp finite.
+    """
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1], dtype=np.float64)
+    z = scale * (K @ q)
+    p = np.exp(z - z.max())
+    return (p @ V) / p.sum()
+
+
+def attention_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                  block_tables: np.ndarray, seq_lens: np.ndarray, scale: float,
+                  num_kv_heads: int, dtype: str) -> np.ndarray:
+    """Paged single-query attention for a batch; float64 [B, num_heads, head_dim].
+
+    q: uint16 bits [B, Hq, d]; caches: uint16 bits [NB, bs, Hkv, d];
+    block_tables: int [B, W]; seq_lens: int [B].  Query head h of sequence s
+    attends over the gathered K/V of KV head h // (Hq / Hkv).
+    """
+    B, Hq, d = q.shape
+    G = Hq // num_kv_heads
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    for s in range(B):
+        L = int(seq_lens[s])
+        for g in range(num_kv_heads):
+            K = gather_sequence(key_cache, block_tables[s], L, g, dtype)
+            V = gather_sequence(value_cache, block_tables[s], L, g, dtype)
+            for h in range(g * G, (g + 1) * G):
+                out[s, h] = softmax_attention(decode_bits(q[s, h], dtype), K, V, scale)
+    return out
+
+
+# --------------------------------------------------------------------------
+# split-K pieces: partial softmax over a slice of positions and its merge
+# --------------------------------------------------------------------------
+def partial_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """(m, l, o) over one slice of positions: m = max z, l = sum exp(z - m), o = sum exp(z - m) V.
+
+    The slice's softmax numerator and denominator relative to its own maximum;
+    ``merge_partials`` recombines slices into the softmax over their union.
+    """
+    z = scale * (K @ q)
+    m = z.max()
+    p = np.exp(z - m)
+    return m, p.sum(), p @ V
+
+
+def merge_partials(ms, ls, os) -> np.ndarray:
+    """Combine slice partials: M = max m_p; out = sum e^(m_p-M) o_p / sum e^(m_p-M) l_p."""
+    ms = np.asarray(ms, dtype=np.float64)
+    M = ms.max()
+    w = np.exp(ms - M)
+    num = sum(wi * np.asarray(oi, dtype=np.float64) for wi, oi in zip(w, os))
+    den = float(np.dot(w, np.asarray(ls, dtype=np.float64)))
+    return num / den
+
+
+# --------------------------------------------------------------------------
+# one decode step: copy-on-write copies, slot writes, attention
+# --------------------------------------------------------------------------
+def decode_step_ref(key_caches, value_caches, copy_pairs, k_new, v_new, slot_mapping,
+                    q, block_tables, seq_lens, scale: float, num_kv_heads: int, dtype: str,
+                    layers=None):
+    """Apply one step to copies of the caches and return (per-layer outputs, caches).
+
+    Order: copy-on-write copies (P2 §3.3, at the fork), then the new tokens'
+    slot writes (P1 §4.2.2), then attention over [0, seq_len) (P4 §2.2).  Every
+    layer gets the same copies and slot writes with its own K/V; ``layers``
+    restricts the attention to a subset of layers.
+    """
+    kcs = [np.array(k, copy=True) for k in key_caches]
+    vcs = [np.array(v, copy=True) for v in value_caches]
+    if copy_pairs is not None and len(copy_pairs):
+        copy_blocks_ref(kcs, vcs, copy_pairs)
+    outs = {}
+    for l in range(len(kcs)):
+        kn = k_new[l] if isinstance(k_new, (list, tuple)) else k_new
+        vn = v_new[l] if isinstance(v_new, (list, tuple)) else v_new
+        append_ref(kcs[l], vcs[l], kn, vn, slot_mapping)
+        if layers is None or l in layers:
+            ql = q[l] if isinstance(q, (list, tuple)) else q
+            outs[l] = attention_ref(ql, kcs[l], vcs[l], block_tables, seq_lens, scale,
+                                    num_kv_heads, dtype)
+    return outs, kcs, vcs
