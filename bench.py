@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Paged decode-attention benchmark (one JSON line on rank 0).
+
+A step is one pass of the decode hot path over one batch: the fork's
+copy-on-write block copies (workloads that fork), then per layer the new
+tokens' slot writes and the paged attention (split-K partitions + merge).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+``value`` is achieved HBM throughput of the step: algorithmic bytes (K/V of
+the valid positions, q, out, block tables, lengths; slot writes; block
+copies) per second, summed over ranks.  Pools are resident in HBM; the
+replicas rotate so consecutive steps never reuse L2 contents.  ``e2e``
+repeats the measurement through the public API with the step's inputs copied
+from pinned host memory and the outputs read back every step.
+``--impl reference`` times the CPU oracle on a bounded sample instead.
+"""
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak); decode tokens/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    p.add_argument("--workload", default="llama3_8b", choices=sorted(W.SPECS))
+    p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- bytes
+def algorithmic_bytes(wl: W.Workload) -> dict:
+    """Algorithmic bytes of one step (one replica)."""
+    s = wl.spec
+    e, Hkv, Hq, d, bs = s.elem_bytes, s.num_kv_heads, s.num_heads, s.head_dim, s.block_size
+    L = wl.seq_lens.astype(np.int64)
+    nb = (L + bs - 1) // bs
+    small = 2 * s.num_seqs * Hq * d * e + 4 * int(nb.sum()) + 4 * s.num_seqs
+    logical = int(2 * L.sum() * Hkv * d * e) + small
+    # unique: each physical (block, slot) read once even if several sequences share it
+    seen = {}
+    for i in range(s.num_seqs):
+        for j in range(int(nb[i])):
+            b = int(wl.block_tables[i, j])
+            seen[b] = max(seen.get(b, 0), min(bs, int(L[i]) - j * bs))
+    unique = int(2 * sum(seen.values()) * Hkv * d * e) + small
+    valid_tok = int((wl.slot_mapping >= 0).sum())
+    append = 2 * 2 * valid_tok * Hkv * d * e + 8 * wl.num_tokens
+    copy = 2 * 2 * len(wl.copy_pairs) * bs * Hkv * d * e * s.num_layers
+    step = copy + s.num_layers * (append + unique)
+    return dict(decode_unique=unique, decode_logical=logical, append=append, copy=copy, step=step)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pkv_decode.cu", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_156_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    or None when there is none or the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m_h = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != decode_source_hash():
+        return None
+    return int(m_t.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle timing
+def time_oracle(wl: W.Workload, pools, seqs, budget_s: float):
+    """Run the oracle (slot writes, then attention) for sequences in ``seqs``,
+    cycling until ``budget_s`` has elapsed; returns (bytes, seconds, sequences)."""
+    import oracle
+
+    spec = wl.spec
+    kc, vc = pools
+    tok_of = {}
+    # the appended tokens of each sequence, in slot_mapping order
+    t = 0
+    for s in range(spec.num_seqs):
+        n = 1
+        if spec.fork is not None:
+            L, P = int(wl.seq_lens[s]), spec.fork[2]
+            Pc = W.blocks_needed(P, spec.block_size) * spec.block_size
+            n = max(1, len(set(range(P, min(L, Pc))) | ({L - 1} if L > P else set())))
+        tok_of[s] = list(range(t, t + n))
+        t += n
+    per = algorithmic_bytes(wl)
+    Hkv, d, e = spec.num_kv_heads, spec.head_dim, spec.elem_bytes
+    done_bytes, done = 0, 0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        s = seqs[i % len(seqs)]
+        idx = tok_of[s]
+        oracle.append_ref(kc, vc, wl.k_new[idx], wl.v_new[idx], wl.slot_mapping[idx])
+        oracle.attention_ref(wl.q[s:s + 1], kc, vc, wl.block_tables[s:s + 1], wl.seq_lens[s:s + 1], wl.scale, Hkv,
+                             spec.dtype)
+        L = int(wl.seq_lens[s])
+        done_bytes += 2 * L * Hkv * d * e + 2 * spec.num_heads * d * e + 4 * W.blocks_needed(L, spec.block_size) + 4
+        done_bytes += 4 * len(idx) * Hkv * d * e + 8 * len(idx)
+        done += 1
+        i += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    del per
+    return done_bytes, time.perf_counter() - t0, done
+
+
+def sample_for_oracle(wl: W.Workload, n: int = 16):
+    rng = np.random.default_rng(99)
+    return sorted(rng.choice(wl.spec.num_seqs, size=min(n, wl.spec.num_seqs), replace=False).tolist())
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- the library arm
+def run_pkv(args, rank, world, local):
+    from paged_kv_cache_156_gb300 import _build
+
+    if local == 0:
+        _build.build()
+    barrier(world)
+    import paged_kv_cache_156_gb300 as pkv
+
+    pkv.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = W.SPECS[args.workload]
+    wl = W.build(spec, values="none")
+    tdt = torch.float16 if spec.dtype == W.F16 else torch.bfloat16
+    nbytes = algorithmic_bytes(wl)
+
+    def dev_bits(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(tdt)
+
+    q, k_new, v_new = dev_bits(wl.q), dev_bits(wl.k_new), dev_bits(wl.v_new)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    tables = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(wl.seq_lens).to(dev)
+    pairs = torch.from_numpy(wl.copy_pairs).to(dev)
+    footprint = wl.pool_bytes_per_layer() * spec.num_layers
+    replicas = max(1, min(4, math.ceil(3 * L2_BYTES / footprint))) if spec.num_layers == 1 else 1
+    if footprint * replicas > 0.6 * torch.cuda.get_device_properties(dev).total_memory:
+        replicas = 1
+    pools = []
+    for r in range(replicas):
+        kcs, vcs = [], []
+        for l in range(spec.num_layers):
+            k, v = W.device_pools(wl, l, dev)
+            kcs.append(k)
+            vcs.append(v)
+        pools.append((kcs, vcs))
+    outs = [torch.empty_like(q) for _ in range(spec.num_layers)]
+    part = args.partition_tokens or pkv.decode_partition_tokens(spec.num_seqs, spec.num_heads, spec.num_kv_heads,
+                                                                spec.head_dim, wl.max_seq_len)
+    ws = pkv.alloc_workspace(spec.num_seqs, spec.num_heads, spec.num_kv_heads, spec.head_dim, wl.max_seq_len, part,
+                             dev)
+    max_parts = math.ceil(wl.max_seq_len / part) if wl.max_seq_len else 1
+    launches_per_step = (1 if len(wl.copy_pairs) else 0) + spec.num_layers * (2 + (1 if max_parts > 1 else 0))
+
+    ev_pairs = []
+
+    def step(i, timed):
+        kcs, vcs = pools[i % replicas]
+        if len(wl.copy_pairs):
+            pkv.copy_blocks(kcs, vcs, pairs)
+        for l in range(spec.num_layers):
+            pkv.paged_kv_append(k_new, v_new, kcs[l], vcs[l], slots)
+            rec = timed and l == 0
+            if rec:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+            pkv.paged_attention_decode(outs[l], q, kcs[l], vcs[l], tables, lens, wl.scale,
+                                       max_seq_len=wl.max_seq_len, workspace=ws, partition_tokens=part)
+            if rec:
+                b.record()
+                ev_pairs.append((a, b))
+
+    for i in range(max(3, args.warmup)):
+        step(i, False)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0, "device error word raised during warm-up"
+
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        step(i, True)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    max_ms = max_over_ranks(elapsed_ms, world)
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_pairs]))
+    assert pkv.device_error() == 0, "device error word raised during the timed region"
+
+    value = world * nbytes["step"] * args.steps / (max_ms / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    dec_gbs = nbytes["decode_unique"] / (dec_ms / 1e3) / 1e9
+    traffic = profiled_traffic(args.workload)
+
+    # ---- end to end: inputs from pinned host memory, outputs read back, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (q, k_new, v_new, slots, tables, lens)]
+        dev_in = [q, k_new, v_new, slots, tables, lens]
+        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        n_e2e = max(3, args.e2e_steps)
+        torch.cuda.synchronize()
+        barrier(world)
+        w0 = time.perf_counter()
+        for i in range(n_e2e):
+            for h, d_ in zip(host_in, dev_in):
+                d_.copy_(h, non_blocking=True)
+            step(i, False)
+            for h, o in zip(host_out, outs):
+                h.copy_(o, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - w0, world)
+        e2e = {"value": round(world * nbytes["step"] * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "ms_per_step": round(e2e_s * 1e3 / n_e2e, 4)}
+
+    # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kc0 = pools[0][0][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).copy()
+        vc0 = pools[0][1][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).copy()
+        seqs = sample_for_oracle(wl)
+        b, sec, n = time_oracle(wl, (kc0, vc0), seqs, args.cpu_seconds)
+        cpu = {"value": round(b / sec / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} sequence decodes (slot writes + attention, layer 0) cycling over {len(seqs)} "
+                         f"sequences of the workload, {sec:.1f} s single-threaded float64 numpy",
+               "nproc": os.cpu_count()}
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) K/V/q, permuted block pools)",
+        "config": {"workload": spec.name, "description": spec.description, "num_seqs": spec.num_seqs,
+                   "num_heads": spec.num_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                   "block_size": spec.block_size, "num_layers": spec.num_layers,
+                   "mean_seq_len": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
+                   "num_blocks": wl.num_blocks, "copy_pairs": int(len(wl.copy_pairs)),
+                   "partition_tokens": part, "max_partitions": max_parts,
+                   "l2": f"inputs larger than L2: {replicas} rotating pool replicas of "
+                         f"{footprint / 1e9:.3f} GB each (L2 {L2_BYTES / 2**20:.0f} MiB)",
+                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "tokens_per_s": round(world * spec.num_seqs * args.steps / (max_ms / 1e3), 1),
+        "step_bytes": nbytes,
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (partition kernel + merge kernel, layer 0)",
+                     "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": nbytes["decode_unique"], "avg_launch_ms": round(dec_ms, 5)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------- the reference arm (CPU oracle)
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    spec = W.SPECS[args.workload]
+    wl = W.build(spec, values="none")
+    seqs = sample_for_oracle(wl, 4)
+    pools = W.host_pools_for(wl, seqs, 0)
+    # size each step: time one sequence, then give each step ~budget/(K+W)
+    b1, s1, _ = time_oracle(wl, [np.array(x, copy=True) for x in pools], seqs[:1], 0.0)
+    per_step_s = min(5.0, max(s1, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle(wl, pools, seqs, per_step_s)
+    tot_b, tot_s, tot_n = 0, 0.0, 0
+    for _ in range(args.steps):
+        b, s, n = time_oracle(wl, pools, seqs, per_step_s)
+        tot_b += b
+        tot_s += s
+        tot_n += n
+    value = tot_b / tot_s / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+            "data": "synthetic (seeded N(0,1), sampled sequences)",
+            "config": {"workload": spec.name, "description": spec.description},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "kind": "oracle", "cores": 1,
+                             "sample": f"{tot_n} sequence decodes over {len(seqs)} sampled sequences, "
+                                       f"~{per_step_s:.2f} s per step, float64 numpy single-threaded",
+                             "nproc": os.cpu_count()},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_pkv(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

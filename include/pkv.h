@@ -1,0 +1,178 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode library (sm_103a, one GPU).
+ *
+ * The library implements the decode-step hot path of PagedAttention as the
+ * following pages describe it (cited by title and section):
+ *
+ *   P1 "vLLM核心概念：PagedAttention原理、KV Cache分页管理、连续批处理、投机解码概览"
+ *   P2 "LLM 推理引擎内部原理：PagedAttention、Continuous Batching 与现代推理架构剖析"
+ *   P3 "LLM 推理优化深度实战：从 PagedAttention 到 Speculative Decoding 的工程架构"
+ *   P4 the tbr8.org PagedAttention article (title not in the extract)
+ *
+ * Memory layout shared by every call (P4 §2.2, the kernel signature's cache
+ * shape): one K pool and one V pool per layer, each a contiguous array
+ *
+ *     cache[num_blocks][block_size][num_kv_heads][head_dim]      (fp16 or bf16)
+ *
+ * Token position t of sequence s lives in physical block
+ * block_tables[s][t / block_size] at offset t % block_size (P4 §2.1).  Its
+ * flat slot is physical_block * block_size + offset (P2 §2.3, append_slot).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates and frees nothing and keeps no per-call state.  Tensors are
+ *     dense, row-major, in the shapes stated, and 16-byte aligned.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  A return of PKV_OK means the launch was
+ *     accepted, not that the kernels finished.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and returns PKV_ERR_INVALID /
+ *     PKV_ERR_UNSUPPORTED / PKV_ERR_WORKSPACE.  A failed launch returns
+ *     PKV_ERR_CUDA.  pkv_last_error() then holds a message (thread-local).
+ *   - Device-side bounds: a block id outside [0, num_blocks) or a slot
+ *     outside [0, num_blocks * block_size) is never dereferenced; the kernel
+ *     skips that access and raises the device error word (pkv_device_error).
+ *     Such inputs give unspecified output values but never a fault.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,      /* bad pointer, size, shape or alignment               */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, block_size, dtype    */
+    PKV_ERR_WORKSPACE = 3,    /* decode workspace missing or too small               */
+    PKV_ERR_CUDA = 4          /* a CUDA runtime call or launch failed                */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Library ABI version (major * 100 + minor). */
+PKV_API int pkv_version(void);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+PKV_API const char* pkv_last_error(void);
+
+/*
+ * paged_kv_append -- write each new token's K and V into its slot.
+ *
+ * P2 §2.3 (BlockEngine.append_slot gives the slot of the token a sequence
+ * generates next) and P1 §4.2.2 ("增长": each new token goes into the current
+ * block, a new block when it is full).  For every t < num_tokens with
+ * slot_mapping[t] >= 0:
+ *     key_cache  [slot / block_size][slot % block_size][:][:] = k[t][:][:]
+ *     value_cache[slot / block_size][slot % block_size][:][:] = v[t][:][:]
+ * bit for bit.  A negative slot is a padding entry and writes nothing.
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim], dtype `dt`
+ *   key_cache,
+ *   value_cache   [num_blocks][block_size][num_kv_heads][head_dim], updated in place
+ *   slot_mapping  int64 [num_tokens]
+ * Slots must be distinct (two tokens writing one slot race).  num_tokens == 0
+ * is a no-op.  head_dim must be a multiple of 8.
+ */
+PKV_API pkv_status pkv_paged_kv_append(const void* k, const void* v, void* key_cache, void* value_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                               int block_size, int num_kv_heads, int head_dim, pkv_dtype dt,
+                               void* stream);
+
+/*
+ * Workspace for pkv_paged_attention_decode: bytes needed for the split-K
+ * partials of a batch, or 0 when every sequence fits one partition.
+ * partition_tokens: 0 picks the size the decode call picks for the same
+ * arguments on the current device; otherwise the caller's partition size.
+ * Returns (size_t)-1 for invalid arguments.
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int max_seq_len, int partition_tokens);
+
+/* Partition size (tokens) pkv_paged_attention_decode uses when passed 0, or -1 on bad arguments. */
+PKV_API int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int max_seq_len);
+
+/*
+ * paged_attention_decode -- one query token per sequence attends over its
+ * paged K/V (GQA).
+ *
+ * P4 §2.2 (paged_attention_kernel: walk the logical blocks, look up each
+ * physical block in the block table, read its K/V rows, stop at seq_len,
+ * score = q.k / sqrt(head_dim), weight V by the softmax of the scores) and
+ * P2 §2.4 (indirect addressing through the block table; softmax and V
+ * weighting follow the scores).  For sequence s and query head h, with
+ * g = h / (num_heads / num_kv_heads) and positions t < seq_lens[s]:
+ *     z_t = scale * <q[s][h], K_t>,   out[s][h] = sum_t softmax(z)_t * V_t
+ * where K_t, V_t are KV head g's rows at position t.  seq_lens[s] == 0 gives
+ * zeros.  Accumulation is fp32; `out` is rounded to nearest even.
+ *
+ *   out           [num_seqs][num_heads][head_dim], dtype `dt`
+ *   q             [num_seqs][num_heads][head_dim], dtype `dt`
+ *   key_cache,
+ *   value_cache   [num_blocks][block_size][num_kv_heads][head_dim]
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                 ceil(seq_lens[s] / block_size) entries of row s are read
+ *   seq_lens      int32 [num_seqs], each in [0, max_seq_len]
+ *   max_seq_len   host-known upper bound of seq_lens (sizes the launch; it
+ *                 must not exceed max_blocks_per_seq * block_size)
+ *   workspace     device scratch of at least
+ *                 pkv_decode_workspace_bytes(...) bytes (may be NULL when that
+ *                 is 0); its contents on entry are ignored
+ *   partition_tokens  0 = automatic; else a multiple of 64 in [64, 4096].
+ *                 Sequences longer than one partition are split into
+ *                 partitions whose partial softmax states are merged by a
+ *                 second kernel (split-K over the sequence).
+ * head_dim in {64, 128}; block_size in {8, 16, 32}; num_heads a multiple of
+ * num_kv_heads.
+ */
+PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                      int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                      void* workspace, size_t workspace_bytes, int partition_tokens,
+                                      void* stream);
+
+/*
+ * copy_blocks -- the copy-on-write block copy at a fork.
+ *
+ * P2 §3.1 (the scheduler output's blocks_to_copy, "用于 Copy-on-Write") and
+ * §3.3; P1 §4.2.2 (a writer to a shared block copies it, then writes); P4 §五.
+ * For every pair i and every layer l:
+ *     key_caches[l][dst_i] = key_caches[l][src_i];  value_caches[l][dst_i] = value_caches[l][src_i]
+ * bit for bit, where (src_i, dst_i) = src_dst_pairs[i].
+ *
+ *   key_caches, value_caches  HOST arrays of num_layers device pointers, each a
+ *                             pool [num_blocks][block_size][num_kv_heads][head_dim]
+ *   src_dst_pairs             DEVICE int64 [num_pairs][2]
+ * Destinations must be distinct and must not appear as a source (the pairs
+ * are applied concurrently).  num_pairs == 0 or num_layers == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                           const int64_t* src_dst_pairs, int64_t num_pairs, int64_t num_blocks,
+                           int block_size, int num_kv_heads, int head_dim, pkv_dtype dt, void* stream);
+
+/*
+ * Device error word: bit 0 = a block id or slot out of range was skipped,
+ * bit 1 = a pipeline wait gave up after its time limit.  Reads the word of
+ * the current device after synchronising it, stores it in *value and, if
+ * `reset` is non-zero, clears it.  Debug/test use; not for the hot path.
+ */
+PKV_API pkv_status pkv_device_error(unsigned int* value, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,189 @@
+"""Python binding of the paged KV-cache decode library (``_lib/libpkv.so``).
+
+Argument marshalling only: every function checks tensor placement, dtype,
+shape and contiguity, then passes raw device pointers and the current CUDA
+stream to the C ABI declared in ``include/pkv.h``.  All work runs in the
+library's CUDA kernels; there is no CPU path.  A missing library raises.
+
+    paged_kv_append(k, v, key_cache, value_cache, slot_mapping)
+    paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_lens, scale, ...)
+    copy_blocks(key_caches, value_caches, src_dst_pairs)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
+
+PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+_DT = {torch.float16: 0, torch.bfloat16: 1}
+
+# every symbol include/pkv.h declares
+ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
+               "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error")
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pkv status {status}: {message}")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library (build it with ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_i, c_i64, c_p, c_sz, c_f = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+    lib.pkv_version.restype = c_i
+    lib.pkv_version.argtypes = []
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_last_error.argtypes = []
+    lib.pkv_paged_kv_append.restype = c_i
+    lib.pkv_paged_kv_append.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i, c_i, c_i, c_i, c_p]
+    lib.pkv_decode_workspace_bytes.restype = c_sz
+    lib.pkv_decode_workspace_bytes.argtypes = [c_i, c_i, c_i, c_i, c_i, c_i]
+    lib.pkv_decode_partition_tokens.restype = c_i
+    lib.pkv_decode_partition_tokens.argtypes = [c_i, c_i, c_i, c_i, c_i]
+    lib.pkv_paged_attention_decode.restype = c_i
+    lib.pkv_paged_attention_decode.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
+                                               c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_copy_blocks.restype = c_i
+    lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p, c_i64, c_i64, c_i, c_i,
+                                    c_i, c_i, c_p]
+    lib.pkv_device_error.restype = c_i
+    lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), c_i]
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != PKV_OK:
+        raise PkvError(status, load().pkv_last_error().decode(errors="replace"))
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _cuda(name, t, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _pool(name, c):
+    _cuda(name, c, (torch.float16, torch.bfloat16), 4)
+    return c.shape  # num_blocks, block_size, num_kv_heads, head_dim
+
+
+def paged_kv_append(k, v, key_cache, value_cache, slot_mapping) -> None:
+    """Write k[t], v[t] ([T, Hkv, d]) into slot slot_mapping[t] (int64; < 0 = skip)."""
+    NB, bs, Hkv, d = _pool("key_cache", key_cache)
+    if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
+        raise ValueError("value_cache must match key_cache")
+    args = [_cuda("k", k, key_cache.dtype, 3), _cuda("v", v, key_cache.dtype, 3), _cuda("key_cache", key_cache),
+            _cuda("value_cache", value_cache), _cuda("slot_mapping", slot_mapping, torch.int64, 1)]
+    T = k.shape[0]
+    if tuple(k.shape) != (T, Hkv, d) or tuple(v.shape) != (T, Hkv, d) or slot_mapping.shape[0] != T:
+        raise ValueError("k, v must be [T, num_kv_heads, head_dim] and slot_mapping [T]")
+    _check(load().pkv_paged_kv_append(*args, T, NB, bs, Hkv, d, _DT[key_cache.dtype], _stream(key_cache)))
+
+
+def decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) -> int:
+    return int(load().pkv_decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len))
+
+
+def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens=0) -> int:
+    n = load().pkv_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid decode shape")
+    return int(n)
+
+
+def alloc_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens=0, device="cuda"):
+    """A device buffer of the size the decode call needs (None if it needs none)."""
+    n = decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, block_size=None,
+                           num_kv_heads=None, max_seq_len=None, workspace=None, partition_tokens=0) -> None:
+    """out[s, h] = softmax(scale * q[s, h] . K) V over positions [0, seq_lens[s]) of KV head h // G.
+
+    q, out: [B, Hq, d]; caches [NB, bs, Hkv, d]; block_tables int32 [B, W]; seq_lens int32 [B].
+    ``max_seq_len`` is the host-known bound of seq_lens (read from the device
+    if omitted, which synchronises).  ``workspace``: see ``alloc_workspace``.
+    """
+    NB, bs, Hkv, d = _pool("key_cache", key_cache)
+    if block_size is not None and block_size != bs:
+        raise ValueError(f"block_size {block_size} != cache block size {bs}")
+    if num_kv_heads is not None and num_kv_heads != Hkv:
+        raise ValueError(f"num_kv_heads {num_kv_heads} != cache heads {Hkv}")
+    if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
+        raise ValueError("value_cache must match key_cache")
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d):
+        raise ValueError("q and out must be [B, num_heads, head_dim]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    ptrs = [_cuda("out", out, key_cache.dtype), _cuda("q", q, key_cache.dtype), _cuda("key_cache", key_cache),
+            _cuda("value_cache", value_cache), _cuda("block_tables", block_tables, torch.int32, 2)]
+    _cuda("seq_lens", seq_lens, torch.int32, 1)
+    if block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_tables / seq_lens batch mismatch")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_attention_decode(
+        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
+        NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
+
+
+def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:
+    """For each (src, dst) row of src_dst_pairs (int64 [Np, 2]): every layer's block dst = block src."""
+    if isinstance(key_caches, torch.Tensor):
+        key_caches, value_caches = [key_caches], [value_caches]
+    if len(key_caches) != len(value_caches) or not key_caches:
+        raise ValueError("need the same non-zero number of key and value caches")
+    shape, dt = key_caches[0].shape, key_caches[0].dtype
+    for i, (kc, vc) in enumerate(zip(key_caches, value_caches)):
+        _pool(f"key_caches[{i}]", kc)
+        _pool(f"value_caches[{i}]", vc)
+        if kc.shape != shape or vc.shape != shape or kc.dtype != dt or vc.dtype != dt:
+            raise ValueError("all caches must share shape and dtype")
+    _cuda("src_dst_pairs", src_dst_pairs, torch.int64, 2)
+    if src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [Np, 2]")
+    n = len(key_caches)
+    karr = (ctypes.c_void_p * n)(*[kc.data_ptr() for kc in key_caches])
+    varr = (ctypes.c_void_p * n)(*[vc.data_ptr() for vc in value_caches])
+    NB, bs, Hkv, d = shape
+    _check(load().pkv_copy_blocks(karr, varr, n, ctypes.c_void_p(src_dst_pairs.data_ptr()), src_dst_pairs.shape[0],
+                                  NB, bs, Hkv, d, _DT[dt], _stream(key_caches[0])))
+
+
+def device_error(reset: bool = True) -> int:
+    """The device error word (synchronises the device): bit 0 out-of-range id skipped, bit 1 wait timeout."""
+    v = ctypes.c_uint(0)
+    _check(load().pkv_device_error(ctypes.byref(v), 1 if reset else 0))
+    return int(v.value)

@@ -1,0 +1,318 @@
+// The C ABI (include/pkv.h): host-side validation, TMA descriptors, the
+// split-K partition choice and dispatch to the kernels.  No torch types, no
+// allocation, no state carried between calls beyond per-device caches of
+// immutable facts (SM count, the error word's address, configured kernels).
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+// Device error word (bit meanings in include/pkv.h, pkv_device_error).
+__device__ unsigned int g_pkv_error_word;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pkv_status ok() {
+    g_msg[0] = '\0';
+    return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+unsigned* g_err_ptr[kMaxDevices];
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+int sm_count_of(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+// Address of the error word on the current device (looked up once per device).
+unsigned* error_word(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pkv_error_word) == cudaSuccess) g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+// TMA descriptor of one pool [num_blocks][block_size][num_kv_heads][head_dim]
+// (16-bit elements).  One box is one (physical block, KV head) tile:
+// block_size rows of 64 elements (128 bytes), 128-byte swizzled in shared memory.
+pkv_status encode_pool(CUtensorMap* map, const void* base, int64_t num_blocks, int bs, int hkv, int d) {
+    auto enc = encode_fn();
+    if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(bs),
+                          static_cast<cuuint64_t>(num_blocks)};
+    cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(hkv) * d * e,
+                             static_cast<cuuint64_t>(bs) * hkv * d * e};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(bs), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return PKV_OK;
+}
+
+bool valid_dtype(pkv_dtype dt) { return dt == PKV_F16 || dt == PKV_BF16; }
+bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32; }
+
+constexpr int kChunk = 64;
+constexpr int kMaxPartition = 4096;
+
+// Partition size for a decode batch: 512 positions, halved (down to 128)
+// while the batch would give fewer than two CTAs per SM.  Short batches end
+// up as a single partition per sequence (no merge pass).
+int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_seq_len, int sms) {
+    int p = 512;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads * head_groups;
+    while (p > 128 && pairs * ((max_seq_len + p - 1) / p) < 2LL * (sms > 0 ? sms : 148)) p >>= 1;
+    return p;
+}
+
+pkv_status check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len) {
+    if (num_seqs < 0 || num_seqs > 65535) return fail(PKV_ERR_INVALID, "num_seqs %d outside [0, 65535]", num_seqs);
+    if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID, "num_heads %d must be a positive multiple of num_kv_heads %d", num_heads,
+                    num_kv_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", head_dim);
+    if (max_seq_len < 0) return fail(PKV_ERR_INVALID, "max_seq_len %d < 0", max_seq_len);
+    return PKV_OK;
+}
+
+int resolve_partition(int num_seqs, int num_heads, int num_kv_heads, int max_seq_len, int partition_tokens) {
+    const int group = num_heads / num_kv_heads;
+    const int hg = (group + 7) / 8;
+    if (partition_tokens > 0) return partition_tokens;
+    return choose_partition(num_seqs, num_kv_heads, hg, max_seq_len, sm_count_of(current_device()));
+}
+
+size_t workspace_for(int num_seqs, int num_heads, int head_dim, int max_seq_len, int part) {
+    const int64_t max_parts = (static_cast<int64_t>(max_seq_len) + part - 1) / part;
+    if (max_parts <= 1) return 0;
+    const int64_t sh = static_cast<int64_t>(num_seqs) * num_heads * max_parts;
+    const size_t o_bytes = static_cast<size_t>(sh) * head_dim * sizeof(float);
+    const size_t ml_bytes = static_cast<size_t>(sh) * 2 * sizeof(float);
+    return ((o_bytes + 255) & ~size_t(255)) + ml_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_last_error(void) { return g_msg; }
+
+pkv_status pkv_paged_kv_append(const void* k, const void* v, void* key_cache, void* value_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                               int block_size, int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID, "num_tokens %lld < 0", static_cast<long long>(num_tokens));
+    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
+    if (num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0)
+        return fail(PKV_ERR_INVALID, "num_kv_heads %d / head_dim %d (head_dim must be a positive multiple of 8)",
+                    num_kv_heads, head_dim);
+    if (block_size <= 0 || num_blocks <= 0)
+        return fail(PKV_ERR_INVALID, "block_size %d / num_blocks %lld", block_size, static_cast<long long>(num_blocks));
+    if (num_tokens == 0) return ok();
+    if (!k || !v || !key_cache || !value_cache || !slot_mapping) return fail(PKV_ERR_INVALID, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return fail(PKV_ERR_INVALID, "tensors must be 16-byte aligned (slot_mapping 8-byte)");
+    const int dev = current_device();
+    pkv::AppendArgs a;
+    a.k = static_cast<const uint4*>(k);
+    a.v = static_cast<const uint4*>(v);
+    a.key_cache = static_cast<uint4*>(key_cache);
+    a.value_cache = static_cast<uint4*>(value_cache);
+    a.slots = slot_mapping;
+    a.num_tokens = num_tokens;
+    a.num_slots = num_blocks * block_size;
+    a.row_vecs = num_kv_heads * head_dim * 2 / 16;
+    a.err = error_word(dev);
+    cudaError_t e = pkv::launch_append(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len,
+                                  int partition_tokens) {
+    if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) != PKV_OK) return (size_t)-1;
+    if (partition_tokens < 0 || partition_tokens > kMaxPartition || partition_tokens % kChunk != 0)
+        return (size_t)-1;
+    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens);
+    return workspace_for(num_seqs, num_heads, head_dim, max_seq_len, part);
+}
+
+int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len) {
+    if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) != PKV_OK) return -1;
+    return resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, 0);
+}
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                      int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt, void* workspace,
+                                      size_t workspace_bytes, int partition_tokens, void* stream) {
+    pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
+    if (st != PKV_OK) return st;
+    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
+    if (!valid_block_size(block_size)) return fail(PKV_ERR_UNSUPPORTED, "block_size %d not built (8, 16, 32)", block_size);
+    if (num_blocks <= 0 || num_blocks > (int64_t(1) << 31))
+        return fail(PKV_ERR_INVALID, "num_blocks %lld outside [1, 2^31]", static_cast<long long>(num_blocks));
+    if (max_blocks_per_seq < 0 || static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+        return fail(PKV_ERR_INVALID, "max_seq_len %d exceeds max_blocks_per_seq %d * block_size %d", max_seq_len,
+                    max_blocks_per_seq, block_size);
+    if (!isfinite(scale)) return fail(PKV_ERR_INVALID, "scale is not finite");
+    if (partition_tokens < 0 || partition_tokens > kMaxPartition || partition_tokens % kChunk != 0)
+        return fail(PKV_ERR_INVALID, "partition_tokens %d: 0 or a multiple of 64 up to 4096", partition_tokens);
+    if (num_seqs == 0) return ok();
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !seq_lens)
+        return fail(PKV_ERR_INVALID, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned; tables and lengths 4-byte");
+
+    const int dev = current_device();
+    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens);
+    const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
+    if (max_parts > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many partitions (%lld)", static_cast<long long>(max_parts));
+    const size_t need = workspace_for(num_seqs, num_heads, head_dim, max_seq_len, part);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : size_t(0));
+
+    CUtensorMap tmk, tmv;
+    if ((st = encode_pool(&tmk, key_cache, num_blocks, block_size, num_kv_heads, head_dim)) != PKV_OK) return st;
+    if ((st = encode_pool(&tmv, value_cache, num_blocks, block_size, num_kv_heads, head_dim)) != PKV_OK) return st;
+
+    pkv::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    const int64_t sh = static_cast<int64_t>(num_seqs) * num_heads * max_parts;
+    a.ws_o = need ? static_cast<float*>(workspace) : nullptr;
+    a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                                ((static_cast<size_t>(sh) * head_dim * sizeof(float) + 255) & ~size_t(255)))
+                   : nullptr;
+    a.err = error_word(dev);
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.head_groups = (a.group + 7) / 8;
+    a.block_size = block_size;
+    a.part_tokens = part;
+    a.max_parts = static_cast<int>(max_parts);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if (static_cast<int64_t>(num_kv_heads) * a.head_groups > 2147483647LL)
+        return fail(PKV_ERR_UNSUPPORTED, "too many heads");
+    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                           const int64_t* src_dst_pairs, int64_t num_pairs, int64_t num_blocks, int block_size,
+                           int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    if (num_layers < 0 || num_pairs < 0) return fail(PKV_ERR_INVALID, "num_layers / num_pairs < 0");
+    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
+    if (block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+        return fail(PKV_ERR_INVALID, "bad pool shape");
+    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+    if (block_bytes % 16 != 0) return fail(PKV_ERR_INVALID, "block bytes %lld not a multiple of 16", static_cast<long long>(block_bytes));
+    if (num_layers == 0 || num_pairs == 0) return ok();
+    if (!key_caches || !value_caches || !src_dst_pairs) return fail(PKV_ERR_INVALID, "null pointer");
+    if (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) return fail(PKV_ERR_INVALID, "pairs must be 8-byte aligned");
+    for (int l = 0; l < num_layers; ++l)
+        if (!key_caches[l] || !value_caches[l] || !aligned16(key_caches[l]) || !aligned16(value_caches[l]))
+            return fail(PKV_ERR_INVALID, "layer %d cache pointer null or not 16-byte aligned", l);
+    const int dev = current_device();
+    for (int l0 = 0; l0 < num_layers; l0 += pkv::kMaxCopyLayers) {
+        pkv::CopyArgs a;
+        const int n = num_layers - l0 < pkv::kMaxCopyLayers ? num_layers - l0 : pkv::kMaxCopyLayers;
+        for (int i = 0; i < pkv::kMaxCopyLayers; ++i) {
+            a.key[i] = i < n ? static_cast<uint4*>(key_caches[l0 + i]) : nullptr;
+            a.value[i] = i < n ? static_cast<uint4*>(value_caches[l0 + i]) : nullptr;
+        }
+        a.pairs = src_dst_pairs;
+        a.num_pairs = num_pairs;
+        a.num_blocks = num_blocks;
+        a.num_layers = n;
+        a.block_vecs = static_cast<int>(block_bytes / 16);
+        a.err = error_word(dev);
+        cudaError_t e = pkv::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "copy_blocks launch: %s", cudaGetErrorString(e));
+    }
+    return ok();
+}
+
+pkv_status pkv_device_error(unsigned int* value, int reset) {
+    if (!value) return fail(PKV_ERR_INVALID, "null pointer");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "synchronize: %s", cudaGetErrorString(e));
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_pkv_error_word, sizeof(v));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
+    if (reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_pkv_error_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "reset error word: %s", cudaGetErrorString(e));
+    }
+    *value = v;
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol the
+header declares; host-side validation rejects bad arguments before any CUDA
+call.  No compute runs here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_156_gb300 as pkv
+from paged_kv_cache_156_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_symbols() == sorted(pkv.ABI_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(pkv_\w+)$", out, re.M))
+    for name in declared_symbols():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing else leaks out of the library
+    assert exported == set(declared_symbols())
+
+
+def test_version_and_empty_error(lib):
+    assert lib.pkv_version() == 100
+
+
+def test_validation_rejects_before_launch(lib):
+    null = ctypes.c_void_p(0)
+    # unsupported head_dim
+    st = lib.pkv_paged_attention_decode(null, null, null, null, null, 4, null, 2, 10, 8, 2, 96, 16, 10, 1.0, 0,
+                                        null, 0, 0, null)
+    assert st == pkv.PKV_ERR_UNSUPPORTED and b"head_dim" in lib.pkv_last_error()
+    # heads not a multiple of KV heads
+    st = lib.pkv_paged_attention_decode(null, null, null, null, null, 4, null, 2, 10, 7, 2, 128, 16, 10, 1.0, 0,
+                                        null, 0, 0, null)
+    assert st == pkv.PKV_ERR_INVALID
+    # block size not built
+    st = lib.pkv_paged_attention_decode(null, null, null, null, null, 4, null, 2, 10, 8, 2, 128, 12, 10, 1.0, 0,
+                                        null, 0, 0, null)
+    assert st == pkv.PKV_ERR_UNSUPPORTED
+    # max_seq_len beyond the table width
+    st = lib.pkv_paged_attention_decode(null, null, null, null, null, 4, null, 2, 65, 8, 2, 128, 16, 10, 1.0, 0,
+                                        null, 0, 0, null)
+    assert st == pkv.PKV_ERR_INVALID
+    # partition size not a multiple of 64
+    st = lib.pkv_paged_attention_decode(null, null, null, null, null, 4, null, 2, 10, 8, 2, 128, 16, 10, 1.0, 0,
+                                        null, 0, 100, null)
+    assert st == pkv.PKV_ERR_INVALID
+    # null pointers
+    st = lib.pkv_paged_attention_decode(null, null, null, null, null, 4, null, 2, 10, 8, 2, 128, 16, 10, 1.0, 0,
+                                        null, 0, 64, null)
+    assert st == pkv.PKV_ERR_INVALID and b"null" in lib.pkv_last_error()
+    assert lib.pkv_paged_kv_append(null, null, null, null, null, -1, 4, 16, 2, 64, 0, null) == pkv.PKV_ERR_INVALID
+    assert lib.pkv_paged_kv_append(null, null, null, null, null, 3, 4, 16, 2, 64, 0, null) == pkv.PKV_ERR_INVALID
+    assert lib.pkv_paged_kv_append(null, null, null, null, null, 3, 4, 16, 2, 64, 7, null) == pkv.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_copy_blocks(None, None, -1, null, 1, 4, 16, 2, 64, 0, null) == pkv.PKV_ERR_INVALID
+    # empty work is accepted without touching the device
+    assert lib.pkv_paged_kv_append(null, null, null, null, null, 0, 4, 16, 2, 64, 0, null) == pkv.PKV_OK
+    assert lib.pkv_copy_blocks(None, None, 0, null, 0, 4, 16, 2, 64, 0, null) == pkv.PKV_OK
+
+
+def test_workspace_formula(lib):
+    # explicit partition sizes need no device query
+    B, Hq, Hkv, d = 16, 64, 8, 128
+    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 512, 512) == 0        # one partition: no partials
+    n = lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 4096, 512)
+    sh = B * Hq * 8
+    assert n == ((sh * d * 4 + 255) // 256) * 256 + sh * 8
+    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, 96, 4096, 512) == ctypes.c_size_t(-1).value
+    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 4096, 100) == ctypes.c_size_t(-1).value
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    t = torch.zeros(4, 16, 2, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        pkv.paged_kv_append(torch.zeros(1, 2, 64, dtype=torch.float16), torch.zeros(1, 2, 64, dtype=torch.float16),
+                            t, t, torch.zeros(1, dtype=torch.int64))

@@ -105,7 +105,7 @@ SPECS = {
         description="Llama-2-70B-shaped layer: 128 seqs lognormal(500,1.2) in [32,8192], 64 q / 8 kv, d128, bs16, fp16"),
     "llama2_70b_mixed_bs32": Spec(
         "llama2_70b_mixed_bs32", 128, 64, 8, 128, 32, F16, 1003, ("lognormal", 500.0, 1.2, 32, 8192),
-        description="as llama2_70b_mixed_bs16 at block_size 32 (same lengths and values)"),
+        description="as llama2_70b_mixed_bs16 at block_size 32 (same lengths, its own pool)"),
     "cow_fork": Spec(
         "cow_fork", 768, 32, 8, 128, 8, F16, 1004, ("fork",), num_layers=1,
         fork=(256, 3, 1024, 0, 512),
@@ -349,3 +349,27 @@ def device_pools(wl: Workload, layer: int, device="cuda"):
         x[mask] = float("nan")
         out.append(x)
     return out[0], out[1]
+
+
+def host_pools_for(wl: Workload, seqs, layer: int = 0):
+    """One layer's host pools with values only in the blocks ``seqs`` use (rest NaN).
+
+    For timing the CPU oracle on a sample without drawing the whole pool.
+    Values come from a generator seeded by (layer seed, block id), so a block's
+    contents do not depend on which sample asked for it.
+    """
+    spec = wl.spec
+    nan = np.uint16(NAN_BITS[spec.dtype])
+    kc = np.full(wl.pool_shape(), nan, dtype=np.uint16)
+    vc = np.full(wl.pool_shape(), nan, dtype=np.uint16)
+    blk_shape = wl.pool_shape()[1:]
+    for s in seqs:
+        nb = blocks_needed(int(wl.seq_lens[s]), spec.block_size)
+        for b in wl.block_tables[s, :nb]:
+            b = int(b)
+            rng = np.random.default_rng((wl.layer_seeds[layer], b))
+            kc[b] = normal_bits(rng, blk_shape, spec.dtype)
+            vc[b] = normal_bits(rng, blk_shape, spec.dtype)
+            kc[b][~wl.valid_slots[b]] = nan
+            vc[b][~wl.valid_slots[b]] = nan
+    return kc, vc
