@@ -249,7 +249,7 @@ def run_pkv(args, rank, world, local):
     lens = torch.from_numpy(wl.seq_lens).to(dev)
     pairs = torch.from_numpy(wl.copy_pairs).to(dev)
     footprint = wl.pool_bytes_per_layer() * spec.num_layers
-    replicas = max(1, min(4, math.ceil(3 * L2_BYTES / footprint))) if spec.num_layers == 1 else 1
+    replicas = max(2, min(4, math.ceil(3 * L2_BYTES / footprint))) if spec.num_layers == 1 else 1
     if footprint * replicas > 0.6 * torch.cuda.get_device_properties(dev).total_memory:
         replicas = 1
     pools = []

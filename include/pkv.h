@@ -90,8 +90,8 @@ PKV_API pkv_status pkv_paged_kv_append(const void* k, const void* v, void* key_c
                                void* stream);
 
 /*
- * Workspace for pkv_paged_attention_decode: bytes needed for the split-K
- * partials of a batch, or 0 when every sequence fits one partition.
+ * Workspace for pkv_paged_attention_decode: bytes needed for its work counter,
+ * per-(sequence, head group) merge tickets and the split-K partials (never 0).
  * partition_tokens: 0 picks the size the decode call picks for the same
  * arguments on the current device; otherwise the caller's partition size.
  * Returns (size_t)-1 for invalid arguments.
@@ -126,13 +126,15 @@ PKV_API int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_
  *   seq_lens      int32 [num_seqs], each in [0, max_seq_len]
  *   max_seq_len   host-known upper bound of seq_lens (sizes the launch; it
  *                 must not exceed max_blocks_per_seq * block_size)
- *   workspace     device scratch of at least
- *                 pkv_decode_workspace_bytes(...) bytes (may be NULL when that
- *                 is 0); its contents on entry are ignored
+ *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
+ *                 bytes, 16-byte aligned; its contents on entry are ignored
+ *                 (the call zeroes the counters it needs on `stream`).  Calls
+ *                 that share a workspace must be ordered on one stream.
  *   partition_tokens  0 = automatic; else a multiple of 64 in [64, 4096].
  *                 Sequences longer than one partition are split into
- *                 partitions whose partial softmax states are merged by a
- *                 second kernel (split-K over the sequence).
+ *                 partitions whose partial softmax states are merged in the
+ *                 same launch by the last partition to finish (split-K over
+ *                 the sequence).
  * head_dim in {64, 128}; block_size in {8, 16, 32}; num_heads a multiple of
  * num_kv_heads.
  */

@@ -118,9 +118,9 @@ def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_
 
 
 def alloc_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens=0, device="cuda"):
-    """A device buffer of the size the decode call needs (None if it needs none)."""
+    """A device buffer of the size the decode call needs."""
     n = decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens)
-    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, block_size=None,
@@ -129,7 +129,8 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_len
 
     q, out: [B, Hq, d]; caches [NB, bs, Hkv, d]; block_tables int32 [B, W]; seq_lens int32 [B].
     ``max_seq_len`` is the host-known bound of seq_lens (read from the device
-    if omitted, which synchronises).  ``workspace``: see ``alloc_workspace``.
+    if omitted, which synchronises).  ``workspace``: see ``alloc_workspace``
+    (allocated here when omitted).
     """
     NB, bs, Hkv, d = _pool("key_cache", key_cache)
     if block_size is not None and block_size != bs:
@@ -150,10 +151,10 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_len
     _cuda("seq_lens", seq_lens, torch.int32, 1)
     if block_tables.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_tables / seq_lens batch mismatch")
-    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
-    if workspace is not None:
-        ws_ptr = _cuda("workspace", workspace)
-        ws_bytes = workspace.numel() * workspace.element_size()
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
+    ws_ptr = _cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().pkv_paged_attention_decode(
         *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
         NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))

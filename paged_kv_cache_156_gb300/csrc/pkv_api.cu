@@ -108,11 +108,13 @@ bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32; }
 constexpr int kChunk = 64;
 constexpr int kMaxPartition = 4096;
 
-// Partition size for a decode batch: 512 positions, halved (down to 128)
-// while the batch would give fewer than two CTAs per SM.  Short batches end
-// up as a single partition per sequence (no merge pass).
+// Partition size for a decode batch: 1024 positions (measured best on the
+// 8B- and 70B-shaped batches), grown while a sequence would need more than
+// 512 partitions, halved (down to 128) while the batch would give fewer than
+// two CTAs per SM.  Short batches end up as a single partition per sequence.
 int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_seq_len, int sms) {
-    int p = 512;
+    int p = 1024;
+    while (p < kMaxPartition && (max_seq_len + p - 1) / p > 512) p <<= 1;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads * head_groups;
     while (p > 128 && pairs * ((max_seq_len + p - 1) / p) < 2LL * (sms > 0 ? sms : 148)) p >>= 1;
     return p;
@@ -136,13 +138,10 @@ int resolve_partition(int num_seqs, int num_heads, int num_kv_heads, int max_seq
     return choose_partition(num_seqs, num_kv_heads, hg, max_seq_len, sm_count_of(current_device()));
 }
 
-size_t workspace_for(int num_seqs, int num_heads, int head_dim, int max_seq_len, int part) {
-    const int64_t max_parts = (static_cast<int64_t>(max_seq_len) + part - 1) / part;
-    if (max_parts <= 1) return 0;
-    const int64_t sh = static_cast<int64_t>(num_seqs) * num_heads * max_parts;
-    const size_t o_bytes = static_cast<size_t>(sh) * head_dim * sizeof(float);
-    const size_t ml_bytes = static_cast<size_t>(sh) * 2 * sizeof(float);
-    return ((o_bytes + 255) & ~size_t(255)) + ml_bytes;
+size_t workspace_for(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len, int part) {
+    const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
+    return pkv::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, static_cast<int>(max_parts))
+        .total();
 }
 
 }  // namespace
@@ -190,7 +189,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
     if (partition_tokens < 0 || partition_tokens > kMaxPartition || partition_tokens % kChunk != 0)
         return (size_t)-1;
     const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens);
-    return workspace_for(num_seqs, num_heads, head_dim, max_seq_len, part);
+    return workspace_for(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, part);
 }
 
 int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len) {
@@ -225,11 +224,18 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     const int dev = current_device();
     const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens);
     const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
-    if (max_parts > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many partitions (%lld)", static_cast<long long>(max_parts));
-    const size_t need = workspace_for(num_seqs, num_heads, head_dim, max_seq_len, part);
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    if (max_parts > 512)
+        return fail(PKV_ERR_UNSUPPORTED, "%lld partitions per sequence (at most 512; use a larger partition_tokens)",
+                    static_cast<long long>(max_parts));
+    const pkv::DecodeWorkspace lay =
+        pkv::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, static_cast<int>(max_parts));
+    const size_t need = lay.total();
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
                     workspace ? workspace_bytes : size_t(0));
+    const int group = num_heads / num_kv_heads;
+    if (static_cast<int64_t>(num_kv_heads) * ((group + 7) / 8) * max_parts * num_seqs >= (int64_t(1) << 31))
+        return fail(PKV_ERR_UNSUPPORTED, "too many work items");
 
     CUtensorMap tmk, tmv;
     if ((st = encode_pool(&tmk, key_cache, num_blocks, block_size, num_kv_heads, head_dim)) != PKV_OK) return st;
@@ -240,11 +246,11 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     a.q = q;
     a.block_tables = block_tables;
     a.seq_lens = seq_lens;
-    const int64_t sh = static_cast<int64_t>(num_seqs) * num_heads * max_parts;
-    a.ws_o = need ? static_cast<float*>(workspace) : nullptr;
-    a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                                ((static_cast<size_t>(sh) * head_dim * sizeof(float) + 255) & ~size_t(255)))
-                   : nullptr;
+    char* ws = static_cast<char*>(workspace);
+    a.work_counter = reinterpret_cast<unsigned*>(ws);
+    a.tickets = a.work_counter + 1;
+    a.ws_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ticket_bytes) : nullptr;
+    a.ws_ml = max_parts > 1 ? reinterpret_cast<float2*>(ws + lay.ticket_bytes + lay.o_bytes) : nullptr;
     a.err = error_word(dev);
     a.num_blocks = num_blocks;
     a.max_blocks_per_seq = max_blocks_per_seq;
@@ -257,9 +263,8 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     a.part_tokens = part;
     a.max_parts = static_cast<int>(max_parts);
     a.scale_log2 = scale * 1.4426950408889634f;
-    if (static_cast<int64_t>(num_kv_heads) * a.head_groups > 2147483647LL)
-        return fail(PKV_ERR_UNSUPPORTED, "too many heads");
-    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
+    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, lay.ticket_bytes,
+                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return ok();
 }

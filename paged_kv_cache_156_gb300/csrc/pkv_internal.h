@@ -39,6 +39,8 @@ struct DecodeArgs {
     const void* q;                   // [B][Hq][D]
     const int32_t* block_tables;     // [B][max_blocks_per_seq]
     const int32_t* seq_lens;         // [B]
+    unsigned* work_counter;          // next work item (zeroed before each launch)
+    unsigned* tickets;               // [B][num_kv_heads * head_groups] finished partitions (zeroed)
     float* ws_o;                     // [B][Hq][max_parts][D] unnormalised partial outputs
     float2* ws_ml;                   // [B][Hq][max_parts] (running max in log2 units, sum)
     unsigned* err;
@@ -55,9 +57,19 @@ struct DecodeArgs {
     float scale_log2;                // scale * log2(e)
 };
 
-// dtype: 0 = f16, 1 = bf16.  Launches the partition kernel and, when
-// max_parts > 1, the merge kernel.
+// Workspace layout of one decode call: [counter + tickets | partial outputs | (max, sum) pairs],
+// each region 256-byte aligned.  Only the first region needs zeroing per call.
+struct DecodeWorkspace {
+    size_t ticket_bytes;   // counter + tickets, padded
+    size_t o_bytes;        // partial outputs, padded (0 when max_parts == 1)
+    size_t ml_bytes;       // (max, sum) pairs (0 when max_parts == 1)
+    size_t total() const { return ticket_bytes + o_bytes + ml_bytes; }
+};
+DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_parts);
+
+// dtype: 0 = f16, 1 = bf16.  Zeroes the counters (one memset) and launches
+// the persistent decode kernel, which also merges split partitions.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, cudaStream_t s);
+                          int head_dim, size_t zero_bytes, cudaStream_t s);
 
 }  // namespace pkv

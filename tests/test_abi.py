@@ -82,10 +82,14 @@ def test_validation_rejects_before_launch(lib):
 def test_workspace_formula(lib):
     # explicit partition sizes need no device query
     B, Hq, Hkv, d = 16, 64, 8, 128
-    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 512, 512) == 0        # one partition: no partials
+    pad = lambda x: (x + 255) // 256 * 256
+    tickets = pad(4 * (1 + B * Hkv))          # work counter + one ticket per (sequence, KV head)
+    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 512, 512) == tickets   # one partition: no partials
     n = lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 4096, 512)
     sh = B * Hq * 8
-    assert n == ((sh * d * 4 + 255) // 256) * 256 + sh * 8
+    assert n == tickets + pad(sh * d * 4) + pad(sh * 8)
+    # more than 8 query heads per KV head: one ticket per 8-head group
+    assert lib.pkv_decode_workspace_bytes(2, 64, 2, d, 64, 64) == pad(4 * (1 + 2 * 2 * 4))
     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, 96, 4096, 512) == ctypes.c_size_t(-1).value
     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 4096, 100) == ctypes.c_size_t(-1).value
 
