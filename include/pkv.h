@@ -173,6 +173,42 @@ PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_c
  */
 PKV_API pkv_status pkv_device_error(unsigned int* value, int reset);
 
+/*
+ * paged_attention_decode_static -- pkv_paged_attention_decode for callers that
+ * cannot allocate device memory.
+ *
+ * The source pages have no counterpart: this entry point exists for how the
+ * library is called, not for what it computes.  Some callers have no way to
+ * call cudaMalloc: a plugin inside a host engine that owns the device's whole
+ * memory budget and hands the plugin only its input and output buffers, or a
+ * serving loop that reserves all device memory at start-up and must not
+ * allocate afterwards.  They cannot provide the decode workspace, so this call
+ * uses a scratch array built into the library instead.  It computes exactly
+ * what pkv_paged_attention_decode computes (same arguments, minus workspace),
+ * through the same kernels.
+ *
+ *   - The scratch is a file-scope device array of PKV_STATIC_DECODE_SCRATCH_BYTES
+ *     bytes.  Every GPU that loads the library holds it until the process exits.
+ *   - A batch whose workspace (pkv_decode_workspace_bytes for the same
+ *     arguments) exceeds that size is rejected with PKV_ERR_WORKSPACE and a
+ *     message giving both sizes; nothing is launched.
+ *   - The call allocates and frees nothing.  The first call on a device looks
+ *     up the array's device address (cudaGetSymbolAddress) with that device
+ *     current and caches it; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     the counters a call needs zeroed are cleared on `stream` by the call
+ *     itself.  Calls whose kernels overlap on the GPU (other streams, other
+ *     host threads) race on the array: order them on one stream.
+ */
+#define PKV_STATIC_DECODE_SCRATCH_BYTES ((size_t)32 << 20)
+
+PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* q, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                      int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                      int partition_tokens, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

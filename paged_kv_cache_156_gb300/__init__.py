@@ -25,7 +25,8 @@ _DT = {torch.float16: 0, torch.bfloat16: 1}
 
 # every symbol include/pkv.h declares
 ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
-               "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error")
+               "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
+               "pkv_paged_attention_decode_static")
 
 _lib = None
 
@@ -63,6 +64,9 @@ def load() -> ctypes.CDLL:
                                     c_i, c_i, c_p]
     lib.pkv_device_error.restype = c_i
     lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), c_i]
+    lib.pkv_paged_attention_decode_static.restype = c_i
+    lib.pkv_paged_attention_decode_static.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
+                                                      c_i64, c_f, c_i, c_i, c_p]
     _lib = lib
     return lib
 

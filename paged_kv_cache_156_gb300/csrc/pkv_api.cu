@@ -146,6 +146,13 @@ size_t workspace_for(int num_seqs, int num_heads, int num_kv_heads, int head_dim
 
 }  // namespace
 
+namespace pkv {
+int set_error_message(int st, const char* msg) {
+    snprintf(g_msg, sizeof(g_msg), "%s", msg);
+    return st;
+}
+}  // namespace pkv
+
 extern "C" {
 
 int pkv_version(void) { return 100; }

@@ -72,4 +72,7 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
                           int head_dim, size_t zero_bytes, cudaStream_t s);
 
+// Record `msg` as the calling thread's pkv_last_error() message and return `st`.
+int set_error_message(int st, const char* msg);
+
 }  // namespace pkv
