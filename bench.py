@@ -376,7 +376,7 @@ def run_pkv(args, rank, world, local):
                    "parallelism": f"replicas x{world} (no data-path collective)"},
         "tokens_per_s": round(world * spec.num_seqs * args.steps / (max_ms / 1e3), 1),
         "step_bytes": nbytes,
-        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (partition kernel + merge kernel, layer 0)",
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (paged_attention_decode call: ticket memset + partition kernel with in-kernel split-K merge; layer 0)",
                      "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": nbytes["decode_unique"], "avg_launch_ms": round(dec_ms, 5)},
