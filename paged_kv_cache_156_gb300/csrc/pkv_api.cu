@@ -108,14 +108,32 @@ bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32; }
 constexpr int kChunk = 64;
 constexpr int kMaxPartition = 4096;
 
-// Partition size for a decode batch: 1024 positions (measured best on the
-// 8B- and 70B-shaped batches), grown while a sequence would need more than
-// 512 partitions, halved (down to 128) while the batch would give fewer than
-// two CTAs per SM.  Short batches end up as a single partition per sequence.
-int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_seq_len, int sms) {
+// Partition size for a decode batch.  1024 positions (measured best on the
+// 8B- and 70B-shaped batches), grown while a sequence would need more than 512
+// partitions.  When the batch, taken as max_seq_len long everywhere, would
+// fill fewer than three waves of CTAs, the size in [512, 1024] (multiple of
+// 64) whose last wave is fullest is taken instead (a uniform 16 x 4096 batch
+// at three CTAs per SM: 640).  Below one wave, halved down to 128 while the
+// batch gives fewer than two CTAs per SM.
+int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_seq_len, int sms, int ctas_per_sm) {
     int p = 1024;
     while (p < kMaxPartition && (max_seq_len + p - 1) / p > 512) p <<= 1;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads * head_groups;
+    const int64_t slots = static_cast<int64_t>(sms > 0 ? sms : 148) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    auto waves = [&](int q) { return static_cast<double>(pairs * ((max_seq_len + q - 1) / q)) / slots; };
+    if (p == 1024 && waves(1024) >= 1.0 && waves(1024) < 3.0) {
+        double best = -1.0;
+        int best_p = 1024;
+        for (int q = 1024; q >= 512; q -= 64) {
+            const double w = waves(q);
+            const double fill = w / static_cast<double>(static_cast<int64_t>(w + 0.999999));
+            if (fill > best + 1e-9) {
+                best = fill;
+                best_p = q;
+            }
+        }
+        return best_p;
+    }
     while (p > 128 && pairs * ((max_seq_len + p - 1) / p) < 2LL * (sms > 0 ? sms : 148)) p >>= 1;
     return p;
 }
@@ -131,11 +149,13 @@ pkv_status check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int
     return PKV_OK;
 }
 
-int resolve_partition(int num_seqs, int num_heads, int num_kv_heads, int max_seq_len, int partition_tokens) {
+int resolve_partition(int num_seqs, int num_heads, int num_kv_heads, int max_seq_len, int partition_tokens,
+                      int head_dim) {
     const int group = num_heads / num_kv_heads;
     const int hg = (group + 7) / 8;
     if (partition_tokens > 0) return partition_tokens;
-    return choose_partition(num_seqs, num_kv_heads, hg, max_seq_len, sm_count_of(current_device()));
+    return choose_partition(num_seqs, num_kv_heads, hg, max_seq_len, sm_count_of(current_device()),
+                            pkv::decode_ctas_per_sm(head_dim));
 }
 
 size_t workspace_for(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len, int part) {
@@ -195,13 +215,13 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
     if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) != PKV_OK) return (size_t)-1;
     if (partition_tokens < 0 || partition_tokens > kMaxPartition || partition_tokens % kChunk != 0)
         return (size_t)-1;
-    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens);
+    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens, head_dim);
     return workspace_for(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, part);
 }
 
 int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len) {
     if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) != PKV_OK) return -1;
-    return resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, 0);
+    return resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, 0, head_dim);
 }
 
 pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
@@ -229,7 +249,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
         return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned; tables and lengths 4-byte");
 
     const int dev = current_device();
-    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens);
+    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens, head_dim);
     const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
     if (max_parts > 512)
         return fail(PKV_ERR_UNSUPPORTED, "%lld partitions per sequence (at most 512; use a larger partition_tokens)",
@@ -255,9 +275,12 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     a.seq_lens = seq_lens;
     char* ws = static_cast<char*>(workspace);
     a.work_counter = reinterpret_cast<unsigned*>(ws);
-    a.tickets = a.work_counter + 1;
-    a.ws_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ticket_bytes) : nullptr;
-    a.ws_ml = max_parts > 1 ? reinterpret_cast<float2*>(ws + lay.ticket_bytes + lay.o_bytes) : nullptr;
+    a.n_items = a.work_counter + 1;
+    a.tickets = a.work_counter + 2;
+    a.items = reinterpret_cast<unsigned*>(ws + lay.ticket_bytes);
+    a.ws_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ticket_bytes + lay.item_bytes) : nullptr;
+    a.ws_ml = max_parts > 1 ? reinterpret_cast<float2*>(ws + lay.ticket_bytes + lay.item_bytes + lay.o_bytes)
+                            : nullptr;
     a.err = error_word(dev);
     a.num_blocks = num_blocks;
     a.max_blocks_per_seq = max_blocks_per_seq;
@@ -270,8 +293,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     a.part_tokens = part;
     a.max_parts = static_cast<int>(max_parts);
     a.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, lay.ticket_bytes,
-                                       static_cast<cudaStream_t>(stream));
+    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -36,67 +36,28 @@
 //        M = max_p m_p,  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
 //  * Every wait is an mbarrier wait bounded in wall time; a wait that gives
 //    up raises the error word and the CTA winds down.
-#include <float.h>
 #include <stdlib.h>
 
-#include "pkv_device.cuh"
-#include "pkv_internal.h"
+#include "pkv_decode_common.cuh"
 
 namespace pkv {
 
 namespace {
 
-constexpr int kMaxTable = 512;       // staged table entries: part_tokens (<= 4096) / block_size (>= 8)
-constexpr int kHeadsPerCta = 8;      // mma N
-constexpr int kMaxParts = 512;       // partitions per sequence the in-kernel merge handles
-
-// CW consumer warps each own 16 positions of a chunk of 16 * CW positions.
-template <int D, int CW>
-struct Geo {
-    static constexpr int kChunk = 16 * CW;              // positions per pipeline stage
-    static constexpr int kConsumers = 32 * CW;
-    static constexpr int kThreads = kConsumers + 32;    // plus one producer warp
-    static constexpr int kHalves = D / 64;              // 64-element (128-byte) column planes
-    static constexpr int kPlane = kChunk * 128;         // bytes of one plane of a chunk
-    static constexpr int kStage = kHalves * kPlane;     // bytes of K (or V) of one chunk
-    static constexpr int kScratch = CW * kHeadsPerCta * (D + 2) * 4;                     // warp-merge scratch
-    static constexpr int kMergeScratch = (kHeadsPerCta * kMaxParts + kHeadsPerCta) * 4;  // partition merge
-};
+using dec::Geo;
+using dec::kHeadsPerCta;
+using dec::kMaxTable;
 
 template <int D, int CW, int STAGES>
 struct Smem {
     using G = Geo<D, CW>;
     static constexpr size_t kRing = 2 * STAGES * G::kStage;
-    static constexpr size_t kScratch = (G::kScratch > G::kMergeScratch ? G::kScratch : G::kMergeScratch);
-    static constexpr size_t kArena = kRing > kScratch ? kRing : kScratch;   // the scratch aliases the ring
+    static constexpr size_t kArena = kRing > size_t(G::kScratch) ? kRing : size_t(G::kScratch);  // scratch aliases the ring
     static constexpr size_t kBars = kArena;
     static constexpr size_t kTable = kBars + (2 * STAGES + 1) * sizeof(uint64_t);
     static constexpr size_t kMisc = kTable + kMaxTable * sizeof(int);
     static constexpr size_t kBytes = kMisc + 16;
 };
-
-// Address of 16-byte column chunk `ch` (0..7) of row `row` in a 128B-swizzled
-// plane whose base is 1024-byte aligned: the chunk index is XORed with row % 8.
-__device__ __forceinline__ uint32_t swz(uint32_t plane, int row, int ch) {
-    return plane + row * 128 + ((ch ^ (row & 7)) << 4);
-}
-
-// Bounded wait that also gives up as soon as the CTA's abort flag is raised.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void raise_abort(const DecodeArgs& a, volatile int* abort_flag) {
-    if (!*abort_flag) raise_error(a.err, kErrTimeout);
-    *abort_flag = 1;
-}
 
 template <typename T, int D, int CW, int STAGES>
 __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -104,9 +65,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
                                                                      const DecodeArgs a) {
     using G = Geo<D, CW>;
     using S = Smem<D, CW, STAGES>;
-    using M = Mma<T>;
     constexpr int kChunk = G::kChunk;
-    constexpr int kConsumerWarps = CW;
     constexpr int kConsumers = G::kConsumers;
     constexpr int kThreads = G::kThreads;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -114,7 +73,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     uint8_t* vring = smem + STAGES * G::kStage;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
     uint64_t* empty = full + STAGES;
-    uint64_t* epi = empty + STAGES;               // consumer-group barrier (all 128 consumer threads)
+    uint64_t* epi = empty + STAGES;               // consumer-group barrier (all consumer threads)
     int* tbl = reinterpret_cast<int*>(smem + S::kTable);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kMisc);
     volatile int* merge_flag = abort_flag + 1;
@@ -137,10 +96,10 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     // query fragments (consumers).
     constexpr int kTePerLane = (kMaxTable + 31) / 32;
     int te[kTePerLane];
-    uint32_t qb[D / 16][2];
+    dec::WarpState<D> ws;
     const int first_blk = start / bs;
     const int tcount = min(a.part_tokens / bs, a.max_blocks_per_seq - first_blk);
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         const int32_t* row = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + first_blk;
 #pragma unroll
         for (int k = 0; k < kTePerLane; ++k) {
@@ -157,8 +116,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
             reinterpret_cast<const T*>(a.q) + (static_cast<int64_t>(s) * a.num_heads + h0 + nq) * D);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            qb[ks][0] = n < gc ? __ldg(qrow + (ks * 16 + kq) / 2) : 0u;
-            qb[ks][1] = n < gc ? __ldg(qrow + (ks * 16 + 8 + kq) / 2) : 0u;
+            ws.qb[ks][0] = n < gc ? __ldg(qrow + (ks * 16 + kq) / 2) : 0u;
+            ws.qb[ks][1] = n < gc ? __ldg(qrow + (ks * 16 + 8 + kq) / 2) : 0u;
         }
     }
 
@@ -177,7 +136,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
+            mbar_init(&empty[i], CW);
         }
         mbar_init(epi, kConsumers);
         // the 128B swizzle assumes a 1 KB aligned ring; refuse to run otherwise
@@ -190,7 +149,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     __syncthreads();
 
     // ================================================================ producer warp
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         const int nblk = (end - start + bs - 1) / bs;
 #pragma unroll
         for (int k = 0; k < kTePerLane; ++k) {
@@ -212,8 +171,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % STAGES;
                 const unsigned ph = (c / STAGES) & 1;
-                if (!wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
-                    raise_abort(a, abort_flag);
+                if (!dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
+                    dec::raise_abort(a.err, abort_flag);
                     break;
                 }
                 const int tok0 = start + c * kChunk;
@@ -234,21 +193,12 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     }
 
     // ================================================================ consumer warps
-    float o[D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
-    float mrun0 = -INFINITY, mrun1 = -INFINITY, lrun0 = 0.0f, lrun1 = 0.0f;
-    const float sl2 = a.scale_log2;
-    const int krow = warp * 16 + (lane & 15);                     // ldmatrix row supplied by this lane (K)
-    const int kcol = lane >> 4;                                    // +8 elements
-    const int vrow = warp * 16 + (lane & 7) + ((lane >> 4) << 3);  // (V, transposed load)
-    const int vcol = (lane >> 3) & 1;
-    const int r0 = lane >> 2;                                      // accumulator row (position) of c0/c1
+    dec::reset_state(ws);
     bool ok = !*abort_flag;
     unsigned epi_uses = 0;
-    auto epi_sync = [&]() -> bool {               // all 128 consumer threads, bounded
+    auto epi_sync = [&]() -> bool {               // all consumer threads, bounded
         mbar_arrive(epi);
-        const bool r = wait_or_abort(epi, epi_uses & 1, abort_flag);
+        const bool r = dec::wait_or_abort(epi, epi_uses & 1, abort_flag);
         ++epi_uses;
         return r;
     };
@@ -256,76 +206,17 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c % STAGES;
         const unsigned ph = (c / STAGES) & 1;
-        bool got = wait_or_abort(&full[st], ph, abort_flag);
+        bool got = dec::wait_or_abort(&full[st], ph, abort_flag);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
-            if (lane == 0) raise_abort(a, abort_flag);
+            if (lane == 0) dec::raise_abort(a.err, abort_flag);
             ok = false;
             break;
         }
-        const int tok0 = start + c * kChunk + warp * 16;
-        const int nv = min(16, end - tok0);
-        const uint32_t kst = smem_u32(kring + st * G::kStage);
-        const uint32_t vst = smem_u32(vring + st * G::kStage);
-        if (nv > 0) {
-            if (nv < 16) {
-                // rows past seq_len hold no token: zero their V so 0-weights stay 0
-                const int nz = (16 - nv) * (D / 8);
-                for (int i = lane; i < nz; i += 32) {
-                    const int r = warp * 16 + nv + i / (D / 8);
-                    const int cc = i % (D / 8);
-                    const uint32_t addr = swz(vst + (cc >> 3) * G::kPlane, r, cc & 7);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            // ---- S^T = K Q^T
-            float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t af[4];
-                ldmatrix_x4(af, swz(kst + (ks >> 2) * G::kPlane, krow, (ks & 3) * 2 + kcol));
-                M::run(sacc, af, qb[ks][0], qb[ks][1]);
-            }
-            // ---- online softmax (log2 domain); columns are heads 2*(lane%4) + {0,1}
-            const bool va = r0 < nv, vb = r0 + 8 < nv;
-            const float s0 = va ? sacc[0] * sl2 : -INFINITY;
-            const float s1 = va ? sacc[1] * sl2 : -INFINITY;
-            const float s2 = vb ? sacc[2] * sl2 : -INFINITY;
-            const float s3 = vb ? sacc[3] * sl2 : -INFINITY;
-            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
-            const float al0 = fast_exp2(mrun0 - mn0), al1 = fast_exp2(mrun1 - mn1);
-            mrun0 = mn0;
-            mrun1 = mn1;
-            const uint32_t p01 = M::pack(fast_exp2(s0 - mn0), fast_exp2(s1 - mn1));
-            const uint32_t p23 = M::pack(fast_exp2(s2 - mn0), fast_exp2(s3 - mn1));
-            const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);   // the weights PV actually uses
-            lrun0 = lrun0 * al0 + f01.x + f23.x;
-            lrun1 = lrun1 * al1 + f01.y + f23.y;
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
-            }
-            // ---- O^T += V^T P^T ; P^T fragment = transpose of the score fragment
-            const uint32_t pb0 = movmatrix_trans(p01);
-            const uint32_t pb1 = movmatrix_trans(p23);
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                uint32_t vf[4];
-                ldmatrix_x4_trans(vf, swz(vst + (mt >> 2) * G::kPlane, vrow, (mt & 3) * 2 + vcol));
-                M::run(o[mt], vf, pb0, pb1);
-            }
-        }
+        const int nv = min(16, end - (start + c * kChunk + warp * 16));
+        if (nv > 0)
+            dec::consume_chunk<T, D, CW>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage), nv,
+                                         warp, lane, a.scale_log2);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -338,117 +229,28 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     }
 
     // ================================================= epilogue
-    // merge the four warps' states through shared memory (the ring is free:
-    // every chunk was consumed by every warp, so no copy is still landing)
-    float l0 = lrun0, l1 = lrun1;
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    float* sm_m = reinterpret_cast<float*>(kring);
-    float* sm_l = sm_m + kConsumerWarps * kHeadsPerCta;
-    float* sm_o = sm_l + kConsumerWarps * kHeadsPerCta;
+    // merge the warps' states through shared memory (the ring is free: every
+    // chunk was consumed by every warp, so no copy is still landing)
+    float* scratch = reinterpret_cast<float*>(kring);
     if (!epi_sync()) return;                      // every warp is done reading the ring
-    if (lane < 4) {
-        sm_m[warp * kHeadsPerCta + 2 * lane] = mrun0;
-        sm_m[warp * kHeadsPerCta + 2 * lane + 1] = mrun1;
-        sm_l[warp * kHeadsPerCta + 2 * lane] = l0;
-        sm_l[warp * kHeadsPerCta + 2 * lane + 1] = l1;
-    }
-    {
-        const int hA = 2 * (lane & 3);
-        float* oa = sm_o + (warp * kHeadsPerCta + hA) * D;
-        float* ob = oa + D;
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            const int d0 = mt * 16 + r0;
-            oa[d0] = o[mt][0];
-            ob[d0] = o[mt][1];
-            oa[d0 + 8] = o[mt][2];
-            ob[d0 + 8] = o[mt][3];
-        }
-    }
+    dec::warp_state_to_smem<D, CW>(ws, scratch, warp, lane);
     if (!epi_sync()) return;
     const int64_t sh0 = static_cast<int64_t>(s) * a.num_heads + h0;
-    for (int idx = threadIdx.x; idx < gc * D; idx += kConsumers) {
-        const int hx = idx / D;
-        const int d = idx - hx * D;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, sm_m[w * kHeadsPerCta + hx]);
-        float den = 0.0f, num = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float wt = fast_exp2(sm_m[w * kHeadsPerCta + hx] - mx);
-            den += wt * sm_l[w * kHeadsPerCta + hx];
-            num += wt * sm_o[(w * kHeadsPerCta + hx) * D + d];
-        }
-        const int64_t sh = sh0 + hx;
-        if (nparts == 1) {
-            out[sh * D + d] = T(num / den);
-        } else {
-            a.ws_o[(sh * a.max_parts + part) * D + d] = num;
-            if (d == 0) a.ws_ml[sh * a.max_parts + part] = make_float2(mx, den);
-        }
-    }
+    dec::combine_warps<T, D, CW>(a, scratch, sh0, gc, part, nparts, threadIdx.x);
     if (nparts == 1) return;
-    __threadfence();                              // partials visible device-wide before the ticket
+    // The group barrier orders every thread's partial writes before thread 0's
+    // gpu-scope fence, which releases them all before the ticket.
     if (!epi_sync()) return;
     if (threadIdx.x == 0) {
+        __threadfence();
         const unsigned t = atomicAdd(a.tickets + static_cast<int64_t>(s) * a.num_kv_heads * a.head_groups + hh, 1u);
+        __threadfence();
         *merge_flag = (t == static_cast<unsigned>(nparts - 1));
     }
     if (!epi_sync()) return;
     if (!*merge_flag) return;
-    // Last partition of this (sequence, head group) to finish: merge them all.
-    // Weights 2^(m_p - M) and the denominators first (one warp per head, lanes
-    // over partitions), then every output element sums its partials with the
-    // loads of all its heads in flight together.
-    __threadfence();
-    float* wsm = reinterpret_cast<float*>(kring);              // [8 heads][kMaxParts] weights
-    float* dsm = wsm + kHeadsPerCta * kMaxParts;                // [8 heads] denominators
-    for (int hx = warp; hx < gc; hx += kConsumerWarps) {
-        const float2* ml = a.ws_ml + (sh0 + hx) * a.max_parts;
-        float mx = -INFINITY;
-        for (int p = lane; p < nparts; p += 32) mx = fmaxf(mx, __ldcg(ml + p).x);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float den = 0.0f;
-        for (int p = lane; p < nparts; p += 32) {
-            const float2 e = __ldcg(ml + p);
-            const float w = fast_exp2(e.x - mx);
-            wsm[hx * kMaxParts + p] = w;
-            den += w * e.y;
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        if (lane == 0) dsm[hx] = den;
-    }
-    if (!epi_sync()) return;
-    constexpr int kRows = kConsumers / D > 0 ? kConsumers / D : 1;   // heads covered per pass
-    constexpr int kAcc = (kHeadsPerCta + kRows - 1) / kRows;
-    for (int base = 0; base < D; base += kConsumers) {               // D > kConsumers: several passes over d
-        const int d = base + (kConsumers >= D ? threadIdx.x % D : threadIdx.x);
-        const int hb = kConsumers >= D ? threadIdx.x / D : 0;
-        if (d >= D) continue;
-        float num[kAcc];
-#pragma unroll
-        for (int k = 0; k < kAcc; ++k) num[k] = 0.0f;
-        for (int p = 0; p < nparts; ++p) {
-#pragma unroll
-            for (int k = 0; k < kAcc; ++k) {
-                const int hx = hb + k * kRows;
-                if (hx < gc)
-                    num[k] += wsm[hx * kMaxParts + p] * __ldcg(a.ws_o + ((sh0 + hx) * a.max_parts + p) * D + d);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kAcc; ++k) {
-            const int hx = hb + k * kRows;
-            if (hx < gc) out[(sh0 + hx) * D + d] = T(num[k] / dsm[hx]);
-        }
-    }
+    // last partition of this (sequence, head group) to finish: merge them all
+    dec::merge_partitions<T, D, CW>(a, scratch, sh0, gc, nparts, warp, lane, threadIdx.x, epi_sync);
 }
 
 template <typename T, int D, int CW, int STAGES>
@@ -504,19 +306,51 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_
     auto pad = [](size_t x) { return (x + 255) & ~size_t(255); };
     const int group = num_heads / num_kv_heads;
     const int64_t nh = static_cast<int64_t>(num_kv_heads) * ((group + 7) / 8);
+    const int parts = max_parts > 1 ? max_parts : 1;
     DecodeWorkspace w;
-    w.ticket_bytes = pad(sizeof(unsigned) * (1 + static_cast<size_t>(num_seqs) * nh));
+    w.ticket_bytes = pad(sizeof(unsigned) * (2 + static_cast<size_t>(num_seqs) * nh));
+    w.item_bytes = pad(sizeof(unsigned) * static_cast<size_t>(num_seqs) * parts);
     const size_t sh = static_cast<size_t>(num_seqs) * num_heads * (max_parts > 1 ? max_parts : 0);
     w.o_bytes = pad(sh * head_dim * sizeof(float));
     w.ml_bytes = pad(sh * 2 * sizeof(float));
     return w;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, size_t zero_bytes, cudaStream_t s) {
+namespace {
+template <typename T, int D, int CW, int STAGES>
+int occupancy_of() {
+    constexpr size_t smem = Smem<D, CW, STAGES>::kBytes;
+    auto kern = decode_kernel<T, D, CW, STAGES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Geo<D, CW>::kThreads, smem) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int D>
+int occupancy_cfg(int cw, int st) {
+    if (cw == 2) return st == 2 ? occupancy_of<__half, D, 2, 2>() : st == 4 ? occupancy_of<__half, D, 2, 4>()
+                                                                           : occupancy_of<__half, D, 2, 3>();
+    return st == 3 ? occupancy_of<__half, D, 4, 3>() : st == 4 ? occupancy_of<__half, D, 4, 4>()
+                                                               : occupancy_of<__half, D, 4, 2>();
+}
+}  // namespace
+
+int decode_ctas_per_sm(int head_dim) {
+    static int cache[2] = {-1, -1};               // per head_dim; the same on every GB300
+    const int i = head_dim == 64 ? 0 : 1;
+    if (cache[i] < 0) cache[i] = i == 0 ? occupancy_cfg<64>(consumer_warps(), ring_stages())
+                                        : occupancy_cfg<128>(consumer_warps(), ring_stages());
+    return cache[i];
+}
+
+cudaError_t launch_decode_grid(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                               int head_dim, cudaStream_t s) {
     if (a.num_seqs <= 0) return cudaSuccess;
     if (a.max_parts > 1) {
-        cudaError_t e = cudaMemsetAsync(a.tickets, 0, zero_bytes - sizeof(unsigned), s);
+        const size_t n = sizeof(unsigned) * static_cast<size_t>(a.num_seqs) * a.num_kv_heads * a.head_groups;
+        cudaError_t e = cudaMemsetAsync(a.tickets, 0, n, s);
         if (e != cudaSuccess) return e;
     }
     const int st = ring_stages(), cw = consumer_warps();
@@ -526,6 +360,17 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
     }
     return head_dim == 128 ? launch_cfg<__nv_bfloat16, 128>(a, tmk, tmv, cw, st, s)
                            : launch_cfg<__nv_bfloat16, 64>(a, tmk, tmv, cw, st, s);
+}
+
+// Variant: the grid kernel unless PKV_DECODE_VARIANT=persistent (read once).
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                          int head_dim, cudaStream_t s) {
+    static const bool persistent = [] {
+        const char* e = getenv("PKV_DECODE_VARIANT");
+        return e && e[0] == 'p';
+    }();
+    return persistent ? launch_decode_persistent(a, tmk, tmv, dtype, head_dim, s)
+                      : launch_decode_grid(a, tmk, tmv, dtype, head_dim, s);
 }
 
 }  // namespace pkv

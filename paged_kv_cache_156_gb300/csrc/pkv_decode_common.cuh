@@ -1,0 +1,293 @@
+// Pieces shared by the two decode kernels (grid and persistent): the shared
+// memory geometry of a chunk, the per-chunk consumer arithmetic and the
+// epilogue that merges warps and partitions.  Both kernels therefore compute
+// bit-identical results for the same partition size.
+#pragma once
+
+#include <float.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace dec {
+
+constexpr int kMaxTable = 512;       // staged table entries: part_tokens (<= 4096) / block_size (>= 8)
+constexpr int kHeadsPerCta = 8;      // mma N: query heads served by one CTA
+constexpr int kMaxParts = 512;       // partitions per sequence the in-kernel merge handles
+
+// CW consumer warps each own 16 positions of a chunk of 16 * CW positions.
+template <int D, int CW>
+struct Geo {
+    static constexpr int kChunk = 16 * CW;              // positions per pipeline stage
+    static constexpr int kConsumers = 32 * CW;
+    static constexpr int kThreads = kConsumers + 32;    // plus one producer warp
+    static constexpr int kHalves = D / 64;              // 64-element (128-byte) column planes
+    static constexpr int kPlane = kChunk * 128;         // bytes of one plane of a chunk
+    static constexpr int kStage = kHalves * kPlane;     // bytes of K (or V) of one chunk
+    static constexpr int kScratch = (CW * kHeadsPerCta * (D + 2) + 2 * kHeadsPerCta) * 4;  // merge scratch
+};
+
+// Address of 16-byte column chunk `ch` (0..7) of row `row` in a 128B-swizzled
+// plane whose base is 1024-byte aligned: the chunk index is XORed with row % 8.
+__device__ __forceinline__ uint32_t swz(uint32_t plane, int row, int ch) {
+    return plane + row * 128 + ((ch ^ (row & 7)) << 4);
+}
+
+// Bounded wait that also gives up as soon as the CTA's abort flag is raised.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void raise_abort(unsigned* err, volatile int* abort_flag) {
+    if (!*abort_flag) raise_error(err, kErrTimeout);
+    *abort_flag = 1;
+}
+
+// One consumer warp's running state for one work item: O^T accumulators
+// (d x 8 heads, fp32), running max and sum of its two head columns, and the
+// Q^T operand fragments.
+template <int D>
+struct WarpState {
+    float o[D / 16][4];
+    float m0, m1, l0, l1;
+    uint32_t qb[D / 16][2];
+};
+
+template <int D>
+__device__ __forceinline__ void reset_state(WarpState<D>& w) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) w.o[mt][0] = w.o[mt][1] = w.o[mt][2] = w.o[mt][3] = 0.0f;
+    w.m0 = w.m1 = -INFINITY;
+    w.l0 = w.l1 = 0.0f;
+}
+
+// One warp's 16 positions of a chunk: S^T = K Q^T on the tensor cores, online
+// softmax over those scores (log2 domain, positions >= nv masked), then
+// O^T += V^T P^T.  `warp` selects the 16 rows of the chunk; kst / vst are the
+// stage's K and V ring addresses.
+template <typename T, int D, int CW>
+__device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uint32_t vst, int nv, int warp, int lane,
+                                              float sl2) {
+    using G = Geo<D, CW>;
+    using M = Mma<T>;
+    const int krow = warp * 16 + (lane & 15);                     // ldmatrix row supplied by this lane (K)
+    const int kcol = lane >> 4;                                    // +8 elements
+    const int vrow = warp * 16 + (lane & 7) + ((lane >> 4) << 3);  // (V, transposed load)
+    const int vcol = (lane >> 3) & 1;
+    const int r0 = lane >> 2;                                      // accumulator row (position) of c0/c1
+    if (nv < 16) {
+        // rows past seq_len hold no token: zero their V so 0-weights stay 0
+        const int nz = (16 - nv) * (D / 8);
+        for (int i = lane; i < nz; i += 32) {
+            const int r = warp * 16 + nv + i / (D / 8);
+            const int cc = i % (D / 8);
+            const uint32_t addr = swz(vst + (cc >> 3) * G::kPlane, r, cc & 7);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+        fence_proxy_async_smem();                 // before the async proxy refills this stage
+        __syncwarp();
+    }
+    // ---- S^T = K Q^T
+    float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t af[4];
+        ldmatrix_x4(af, swz(kst + (ks >> 2) * G::kPlane, krow, (ks & 3) * 2 + kcol));
+        M::run(sacc, af, w.qb[ks][0], w.qb[ks][1]);
+    }
+    // ---- online softmax (log2 domain); columns are heads 2*(lane%4) + {0,1}
+    const bool va = r0 < nv, vb = r0 + 8 < nv;
+    const float s0 = va ? sacc[0] * sl2 : -INFINITY;
+    const float s1 = va ? sacc[1] * sl2 : -INFINITY;
+    const float s2 = vb ? sacc[2] * sl2 : -INFINITY;
+    const float s3 = vb ? sacc[3] * sl2 : -INFINITY;
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(w.m0, mx0), mn1 = fmaxf(w.m1, mx1);
+    const float al0 = fast_exp2(w.m0 - mn0), al1 = fast_exp2(w.m1 - mn1);
+    w.m0 = mn0;
+    w.m1 = mn1;
+    const uint32_t p01 = M::pack(fast_exp2(s0 - mn0), fast_exp2(s1 - mn1));
+    const uint32_t p23 = M::pack(fast_exp2(s2 - mn0), fast_exp2(s3 - mn1));
+    const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);   // the weights PV actually uses
+    w.l0 = w.l0 * al0 + f01.x + f23.x;
+    w.l1 = w.l1 * al1 + f01.y + f23.y;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        w.o[mt][0] *= al0;
+        w.o[mt][1] *= al1;
+        w.o[mt][2] *= al0;
+        w.o[mt][3] *= al1;
+    }
+    // ---- O^T += V^T P^T ; P^T fragment = transpose of the score fragment
+    const uint32_t pb0 = movmatrix_trans(p01);
+    const uint32_t pb1 = movmatrix_trans(p23);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t vf[4];
+        ldmatrix_x4_trans(vf, swz(vst + (mt >> 2) * G::kPlane, vrow, (mt & 3) * 2 + vcol));
+        M::run(w.o[mt], vf, pb0, pb1);
+    }
+}
+
+// This warp's (max, sum, O) into the merge scratch: m[CW][8], l[CW][8], o[CW][8][D].
+template <int D, int CW>
+__device__ __forceinline__ void warp_state_to_smem(const WarpState<D>& w, float* scratch, int warp, int lane) {
+    float l0 = w.l0, l1 = w.l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float* sm_m = scratch;
+    float* sm_l = sm_m + CW * kHeadsPerCta;
+    float* sm_o = sm_l + CW * kHeadsPerCta;
+    if (lane < 4) {
+        sm_m[warp * kHeadsPerCta + 2 * lane] = w.m0;
+        sm_m[warp * kHeadsPerCta + 2 * lane + 1] = w.m1;
+        sm_l[warp * kHeadsPerCta + 2 * lane] = l0;
+        sm_l[warp * kHeadsPerCta + 2 * lane + 1] = l1;
+    }
+    const int hA = 2 * (lane & 3);
+    float* oa = sm_o + (warp * kHeadsPerCta + hA) * D;
+    float* ob = oa + D;
+    const int r0 = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        const int d0 = mt * 16 + r0;
+        oa[d0] = w.o[mt][0];
+        ob[d0] = w.o[mt][1];
+        oa[d0 + 8] = w.o[mt][2];
+        ob[d0 + 8] = w.o[mt][3];
+    }
+}
+
+// Combine the warps' states of one item (scratch written and synchronised):
+// a sequence of one partition gets its output; otherwise the partition's
+// (max, sum, unnormalised output) go to the workspace.
+template <typename T, int D, int CW>
+__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* scratch, int64_t sh0, int gc, int part,
+                                              int nparts, int tid) {
+    const float* sm_m = scratch;
+    const float* sm_l = sm_m + CW * kHeadsPerCta;
+    const float* sm_o = sm_l + CW * kHeadsPerCta;
+    T* out = reinterpret_cast<T*>(a.out);
+    for (int idx = tid; idx < gc * D; idx += 32 * CW) {
+        const int hx = idx / D;
+        const int d = idx - hx * D;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) mx = fmaxf(mx, sm_m[w * kHeadsPerCta + hx]);
+        float den = 0.0f, num = 0.0f;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) {
+            const float wt = fast_exp2(sm_m[w * kHeadsPerCta + hx] - mx);
+            den += wt * sm_l[w * kHeadsPerCta + hx];
+            num += wt * sm_o[(w * kHeadsPerCta + hx) * D + d];
+        }
+        const int64_t sh = sh0 + hx;
+        if (nparts == 1) {
+            out[sh * D + d] = T(num / den);
+        } else {
+            a.ws_o[(sh * a.max_parts + part) * D + d] = num;
+            if (d == 0) a.ws_ml[sh * a.max_parts + part] = make_float2(mx, den);
+        }
+    }
+}
+
+// Merge every partition of (sequence, head group) into the output; run by the
+// CTA that took the last ticket.  Phase A (one warp per head): the maximum and
+// the denominator, into msm[8] / dsm[8].  `sync` separates the phases.
+// Phase B: each output element sums its partials with all their loads in flight.
+template <typename T, int D, int CW, typename Sync>
+__device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scratch, int64_t sh0, int gc, int nparts,
+                                                 int warp, int lane, int tid, Sync&& sync) {
+    float* msm = scratch;
+    float* dsm = scratch + kHeadsPerCta;
+    for (int hx = warp; hx < gc; hx += CW) {
+        const float2* ml = a.ws_ml + (sh0 + hx) * a.max_parts;
+        float mx = -INFINITY;
+        for (int p = lane; p < nparts; p += 32) mx = fmaxf(mx, __ldcg(ml + p).x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float den = 0.0f;
+        for (int p = lane; p < nparts; p += 32) {
+            const float2 e = __ldcg(ml + p);
+            den += fast_exp2(e.x - mx) * e.y;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        if (lane == 0) {
+            msm[hx] = mx;
+            dsm[hx] = den;
+        }
+    }
+    if (!sync()) return false;
+    constexpr int kConsumers = 32 * CW;
+    constexpr int kRows = kConsumers / D > 0 ? kConsumers / D : 1;   // heads covered per pass
+    constexpr int kAcc = (kHeadsPerCta + kRows - 1) / kRows;
+    T* out = reinterpret_cast<T*>(a.out);
+    for (int base = 0; base < D; base += kConsumers) {               // D > kConsumers: several passes over d
+        const int d = base + (kConsumers >= D ? tid % D : tid);
+        const int hb = kConsumers >= D ? tid / D : 0;
+        float num[kAcc];
+        float mk[kAcc];
+#pragma unroll
+        for (int k = 0; k < kAcc; ++k) {
+            num[k] = 0.0f;
+            const int hx = hb + k * kRows;
+            mk[k] = hx < gc ? msm[hx] : 0.0f;
+        }
+        // partitions in groups of 4 so that 4 * kAcc independent load pairs are in flight
+        int p = 0;
+        for (; p + 4 <= nparts; p += 4) {
+            float e[4][kAcc], v[4][kAcc];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int k = 0; k < kAcc; ++k) {
+                    const int hx = hb + k * kRows;
+                    const int64_t row = (sh0 + (hx < gc ? hx : 0)) * a.max_parts + p + j;
+                    e[j][k] = __ldcg(reinterpret_cast<const float*>(a.ws_ml + row));
+                    v[j][k] = __ldcg(a.ws_o + row * D + d);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int k = 0; k < kAcc; ++k) num[k] += fast_exp2(e[j][k] - mk[k]) * v[j][k];
+            }
+        }
+        for (; p < nparts; ++p) {
+#pragma unroll
+            for (int k = 0; k < kAcc; ++k) {
+                const int hx = hb + k * kRows;
+                if (hx < gc) {
+                    const int64_t row = (sh0 + hx) * a.max_parts + p;
+                    num[k] += fast_exp2(__ldcg(a.ws_ml + row).x - mk[k]) * __ldcg(a.ws_o + row * D + d);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAcc; ++k) {
+            const int hx = hb + k * kRows;
+            if (hx < gc) out[(sh0 + hx) * D + d] = T(num[k] / dsm[hx]);
+        }
+    }
+    return true;
+}
+
+}  // namespace dec
+}  // namespace pkv

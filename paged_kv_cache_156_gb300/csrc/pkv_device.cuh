@@ -96,6 +96,15 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// Contiguous global -> shared bulk copy (16-byte aligned addresses, size a
+// multiple of 16), completion counted on `bar` (bytes).
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

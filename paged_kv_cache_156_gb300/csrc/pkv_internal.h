@@ -39,8 +39,10 @@ struct DecodeArgs {
     const void* q;                   // [B][Hq][D]
     const int32_t* block_tables;     // [B][max_blocks_per_seq]
     const int32_t* seq_lens;         // [B]
-    unsigned* work_counter;          // next work item (zeroed before each launch)
-    unsigned* tickets;               // [B][num_kv_heads * head_groups] finished partitions (zeroed)
+    unsigned* work_counter;          // next work unit of the persistent variant (zeroed per call)
+    unsigned* n_items;               // items in `items` (written per call by the plan kernel)
+    unsigned* tickets;               // [B][num_kv_heads * head_groups] finished partitions (zeroed per call)
+    unsigned* items;                 // [B * max_parts] (sequence << 9 | partition), largest first
     float* ws_o;                     // [B][Hq][max_parts][D] unnormalised partial outputs
     float2* ws_ml;                   // [B][Hq][max_parts] (running max in log2 units, sum)
     unsigned* err;
@@ -57,20 +59,32 @@ struct DecodeArgs {
     float scale_log2;                // scale * log2(e)
 };
 
-// Workspace layout of one decode call: [counter + tickets | partial outputs | (max, sum) pairs],
-// each region 256-byte aligned.  Only the first region needs zeroing per call.
+// Workspace layout of one decode call:
+//   [work counter, item count, tickets | item list | partial outputs | (max, sum) pairs]
+// each region 256-byte aligned.  Every call re-initialises what it uses.
 struct DecodeWorkspace {
-    size_t ticket_bytes;   // counter + tickets, padded
+    size_t ticket_bytes;   // work counter + item count + tickets, padded
+    size_t item_bytes;     // item list, padded
     size_t o_bytes;        // partial outputs, padded (0 when max_parts == 1)
     size_t ml_bytes;       // (max, sum) pairs (0 when max_parts == 1)
-    size_t total() const { return ticket_bytes + o_bytes + ml_bytes; }
+    size_t total() const { return ticket_bytes + item_bytes + o_bytes + ml_bytes; }
 };
 DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_parts);
 
-// dtype: 0 = f16, 1 = bf16.  Zeroes the counters (one memset) and launches
-// the persistent decode kernel, which also merges split partitions.
+// dtype: 0 = f16, 1 = bf16.  Runs one decode call on stream `s`: either the
+// grid variant (one CTA per work item; a memset zeroes the tickets) or the
+// persistent variant (a plan kernel builds the item list, then CTAs resident
+// on every SM pull items).  Both merge split partitions in-kernel.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, size_t zero_bytes, cudaStream_t s);
+                          int head_dim, cudaStream_t s);
+cudaError_t launch_decode_grid(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                               int head_dim, cudaStream_t s);
+cudaError_t launch_decode_persistent(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                                     int head_dim, cudaStream_t s);
+
+// CTAs of the decode kernel resident per SM on the current device (grid
+// variant, current configuration), or 0 if it cannot be queried.
+int decode_ctas_per_sm(int head_dim);
 
 // Record `msg` as the calling thread's pkv_last_error() message and return `st`.
 int set_error_message(int st, const char* msg);
