@@ -8,10 +8,10 @@
 //  * Decode CTAs stay resident (as many per SM as fit) and pull work units
 //    (item, KV-head group) from an atomic counter, largest items first, so the
 //    last wave is made of the smallest items.
-//  * The producer warp resolves the next unit (list entry, sequence length,
-//    block-table slice) while the current one streams, and bulk-copies the
-//    unit's query rows into shared memory with its first chunk, so a CTA pays
-//    no start-up latency between units.
+//  * A scheduler warp claims and resolves the next unit (list entry, sequence
+//    length, block-table slice) while the TMA warp streams the current one and
+//    bulk-copies each unit's query rows into shared memory with its first
+//    chunk, so a CTA pays no start-up latency between units.
 //  * Shared memory is almost all ring (each stage's K and V contiguous): the
 //    consumers keep the stage of a unit's last chunk and use it as the
 //    epilogue's scratch, releasing it afterwards, so the other stages keep
@@ -106,26 +106,24 @@ struct PSmem {
     static constexpr size_t kQ = kRing;
     static constexpr size_t kInfo = kQ + STAGES * kQSlot;
     static constexpr size_t kBars = kInfo + STAGES * sizeof(ChunkInfo);
-    static constexpr size_t kTable = kBars + (2 * STAGES + 1) * sizeof(uint64_t);
-    static constexpr size_t kMisc = kTable + kMaxTable * sizeof(int);
+    static constexpr size_t kTable = kBars + (2 * STAGES + 1) * sizeof(uint64_t);   // two table slices
+    static constexpr size_t kQueue = kTable + 2 * kMaxTable * sizeof(int);              // two resolved units
+    static constexpr size_t kQBars = kQueue + 2 * 8 * sizeof(int);                       // their full/empty barriers
+    static constexpr size_t kMisc = kQBars + 4 * sizeof(uint64_t);
     static constexpr size_t kBytes = kMisc + 16;
 };
 
-// A resolved work unit as the producer warp holds it (every lane the same
-// values, except `te`: this lane's share of the block-table slice).
-struct Unit {
-    int s, hh, part, L;
-    bool valid;
-};
+// Threads of the persistent kernel: consumers, the TMA warp, the scheduler warp.
+template <int D, int CW>
+constexpr int persistent_threads() { return Geo<D, CW>::kThreads + 32; }
 
 template <typename T, int D, int CW, int STAGES>
-__global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_persistent_kernel(
+__global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
     using G = Geo<D, CW>;
     using S = PSmem<D, CW, STAGES>;
     constexpr int kChunk = G::kChunk;
     constexpr int kConsumers = G::kConsumers;
-    constexpr int kTePerLane = (kMaxTable + 31) / 32;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* qslots = smem + S::kQ;
     ChunkInfo* info = reinterpret_cast<ChunkInfo*>(smem + S::kInfo);
@@ -148,6 +146,11 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_persistent_kernel
             mbar_init(&empty[i], CW);
         }
         mbar_init(epi, kConsumers);
+        uint64_t* qb = reinterpret_cast<uint64_t*>(smem + S::kQBars);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qb[i], 32);                // queue slot i filled (every scheduler lane)
+            mbar_init(&qb[2 + i], 1);             // queue slot i consumed (TMA warp)
+        }
         const bool misaligned = (smem_u32(smem) & 1023u) != 0;
         if (misaligned) raise_error(a.err, kErrTimeout);
         *abort_flag = misaligned;
@@ -155,109 +158,126 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_persistent_kernel
         fence_barrier_init();
     }
     __syncthreads();
+    int* qdesc = reinterpret_cast<int*>(smem + S::kQueue);       // [2][8]: s, hh, part, L, valid
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + S::kQBars);
+    uint64_t* qempty = qfull + 2;
 
-    // ================================================================ producer warp
-    if (warp == CW) {
+    // ================================================================ scheduler warp
+    // Claims one work unit at a time from the atomic counter and resolves it
+    // (item entry -> sequence length and block-table slice) into the free slot
+    // of a two-slot queue.  A slot frees when the TMA warp has issued the unit
+    // it held, so a unit is claimed about one unit ahead of its use: late
+    // enough to balance, early enough to hide the dependent loads.
+    if (warp == CW + 1) {
         const unsigned units = *a.n_items * static_cast<unsigned>(NH);
-        int te[kTePerLane];
-        // resolve a unit: list entry, length, and this lane's table entries
-        auto resolve = [&](unsigned v) -> Unit {
-            Unit u;
-            u.valid = v < units;
-            if (!u.valid) return u;
+        for (unsigned j = 0;; ++j) {
+            const int slot = j & 1;
+            if (!dec::wait_or_abort(&qempty[slot], ((j >> 1) & 1) ^ 1, abort_flag)) {
+                if (lane == 0) dec::raise_abort(a.err, abort_flag);
+                break;
+            }
+            unsigned v = 0;
+            if (lane == 0) v = atomicAdd(a.work_counter, 1u);
+            v = __shfl_sync(0xffffffffu, v, 0);
+            int* d = qdesc + slot * 8;
+            if (v >= units) {
+                if (lane == 0) d[4] = 0;
+                __syncwarp();
+                mbar_arrive(&qfull[slot]);
+                break;
+            }
             const unsigned it = __ldg(a.items + v / NH);
-            u.hh = static_cast<int>(v % NH);
-            u.s = static_cast<int>(it >> kPartBits);
-            u.part = static_cast<int>(it & ((1u << kPartBits) - 1));
-            u.L = __ldg(a.seq_lens + u.s);
-            const int first = u.part * P / bs;
+            const int su = static_cast<int>(it >> kPartBits);
+            const int pu = static_cast<int>(it & ((1u << kPartBits) - 1));
+            const int first = pu * P / bs;
             const int tcount = min(P / bs, a.max_blocks_per_seq - first);
-            const int32_t* row = a.block_tables + static_cast<int64_t>(u.s) * a.max_blocks_per_seq + first;
-#pragma unroll
-            for (int k = 0; k < kTePerLane; ++k) {
-                const int i = lane + 32 * k;
-                te[k] = (32 * k < tcount && i < tcount) ? __ldg(row + i) : 0;
-            }
-            return u;
-        };
-        unsigned vnext = 0;
-        if (lane == 0) vnext = atomicAdd(a.work_counter, 1u);
-        Unit cur = resolve(__shfl_sync(0xffffffffu, vnext, 0));
-        if (lane == 0 && cur.valid) vnext = atomicAdd(a.work_counter, 1u);
-        unsigned c = 0;                          // chunks handed over (lane 0)
-        if (lane == 0) {
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
-        }
-        while (cur.valid && !*abort_flag) {
-            const int start = cur.part * P;
-            const int end = min(cur.L, start + P);
-            const int nparts = (cur.L + P - 1) / P;
-            const int nblk = (end - start + bs - 1) / bs;
-            const int nch = (end - start + kChunk - 1) / kChunk;
-#pragma unroll
-            for (int k = 0; k < kTePerLane; ++k) {
-                const int i = lane + 32 * k;
-                if (32 * k < nblk && i < nblk) {
-                    int b = te[k];
-                    if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
-                        raise_error(a.err, kErrBounds);
-                        b = -1;                  // outside the tensor map: TMA fills zeros, reads nothing
-                    }
-                    tbl[i] = b;
+            const int32_t* row = a.block_tables + static_cast<int64_t>(su) * a.max_blocks_per_seq + first;
+            const int L = __ldg(a.seq_lens + su);
+            const int nblk = min(tcount, (min(L, pu * P + P) - pu * P + bs - 1) / bs);
+            for (int i = lane; i < nblk; i += 32) {
+                int b = __ldg(row + i);
+                if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
+                    raise_error(a.err, kErrBounds);
+                    b = -1;                       // outside the tensor map: TMA fills zeros, reads nothing
                 }
+                tbl[slot * kMaxTable + i] = b;
             }
-            __syncwarp();
-            // look ahead: the next unit's loads land while this one is issued
-            const unsigned vn = __shfl_sync(0xffffffffu, vnext, 0);
-            const Unit nxt = resolve(vn);
-            if (lane == 0 && nxt.valid) vnext = atomicAdd(a.work_counter, 1u);
             if (lane == 0) {
-                const int hg = cur.hh % a.head_groups;
-                const int kvh = cur.hh / a.head_groups;
-                const int h0 = kvh * a.group + hg * kHeadsPerCta;
-                const int gc = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
-                const int per_chunk = kChunk / bs;
-                for (int ci = 0; ci < nch; ++ci, ++c) {
-                    const int st = c % STAGES;
-                    const unsigned ph = (c / STAGES) & 1;
-                    if (!dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
-                        dec::raise_abort(a.err, abort_flag);
-                        break;
-                    }
-                    const int tok0 = start + ci * kChunk;
-                    const int nv = min(kChunk, end - tok0);
-                    const int nb = (nv + bs - 1) / bs;
-                    ChunkInfo& in = info[st];
-                    in.s = cur.s;
-                    in.hh = cur.hh;
-                    in.part = cur.part;
-                    in.nvalid = nv;
-                    in.flags = (ci == 0 ? kFirst : 0) | (ci == nch - 1 ? kLast : 0);
-                    in.nparts = nparts;
-                    const unsigned qbytes = ci == 0 ? static_cast<unsigned>(gc * D * 2) : 0u;
-                    mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * 2 * 2) + qbytes);
-                    if (ci == 0)
-                        bulk_copy_g2s(qslots + st * S::kQSlot,
-                                      reinterpret_cast<const T*>(a.q) +
-                                          (static_cast<int64_t>(cur.s) * a.num_heads + h0) * D,
-                                      qbytes, &full[st]);
-                    for (int j = 0; j < nb; ++j) {
-                        const int pb = tbl[ci * per_chunk + j];
+                d[0] = su;
+                d[1] = static_cast<int>(v % NH);
+                d[2] = pu;
+                d[3] = L;
+                d[4] = 1;
+            }
+            __syncwarp();
+            mbar_arrive(&qfull[slot]);            // every lane releases its table entries and the descriptor
+        }
+        return;
+    }
+
+    // ================================================================ TMA warp
+    // Takes resolved units from the queue and streams their chunks into the ring.
+    if (warp == CW) {
+        if (lane != 0) return;
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        unsigned c = 0;                                            // chunks handed over
+        for (unsigned j = 0; !*abort_flag; ++j) {
+            const int slot = j & 1;
+            if (!dec::wait_or_abort(&qfull[slot], (j >> 1) & 1, abort_flag)) {
+                dec::raise_abort(a.err, abort_flag);
+                break;
+            }
+            const int* d = qdesc + slot * 8;
+            if (!d[4]) break;
+            const int s = d[0], hh = d[1], part = d[2], L = d[3];
+            const int start = part * P;
+            const int end = min(L, start + P);
+            const int nparts = (L + P - 1) / P;
+            const int nch = (end - start + kChunk - 1) / kChunk;
+            const int hg = hh % a.head_groups;
+            const int kvh = hh / a.head_groups;
+            const int h0 = kvh * a.group + hg * kHeadsPerCta;
+            const int gc = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
+            const int per_chunk = kChunk / bs;
+            const int* tb = tbl + slot * kMaxTable;
+            for (int ci = 0; ci < nch; ++ci, ++c) {
+                const int st = c % STAGES;
+                const unsigned ph = (c / STAGES) & 1;
+                if (!dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
+                    dec::raise_abort(a.err, abort_flag);
+                    break;
+                }
+                const int tok0 = start + ci * kChunk;
+                const int nv = min(kChunk, end - tok0);
+                const int nb = (nv + bs - 1) / bs;
+                ChunkInfo& in = info[st];
+                in.s = s;
+                in.hh = hh;
+                in.part = part;
+                in.nvalid = nv;
+                in.flags = (ci == 0 ? kFirst : 0) | (ci == nch - 1 ? kLast : 0);
+                in.nparts = nparts;
+                const unsigned qbytes = ci == 0 ? static_cast<unsigned>(gc * D * 2) : 0u;
+                mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * 2 * 2) + qbytes);
+                if (ci == 0)
+                    bulk_copy_g2s(qslots + st * S::kQSlot,
+                                  reinterpret_cast<const T*>(a.q) + (static_cast<int64_t>(s) * a.num_heads + h0) * D,
+                                  qbytes, &full[st]);
+                for (int jb = 0; jb < nb; ++jb) {
+                    const int pb = tb[ci * per_chunk + jb];
 #pragma unroll
-                        for (int hf = 0; hf < G::kHalves; ++hf) {
-                            uint8_t* kdst = smem + st * S::kStagePair + hf * G::kPlane + j * bs * 128;
-                            tma_load_4d(kdst, &tmk, hf * 64, kvh, 0, pb, &full[st]);
-                            tma_load_4d(kdst + G::kStage, &tmv, hf * 64, kvh, 0, pb, &full[st]);
-                        }
+                    for (int hf = 0; hf < G::kHalves; ++hf) {
+                        uint8_t* kdst = smem + st * S::kStagePair + hf * G::kPlane + jb * bs * 128;
+                        tma_load_4d(kdst, &tmk, hf * 64, kvh, 0, pb, &full[st]);
+                        tma_load_4d(kdst + G::kStage, &tmv, hf * 64, kvh, 0, pb, &full[st]);
                     }
                 }
             }
-            __syncwarp();
-            cur = nxt;
+            mbar_arrive(&qempty[slot]);                            // the slot's table is no longer read
         }
         // end marker: one more stage carrying s = -1
-        if (lane == 0 && !*abort_flag) {
+        if (!*abort_flag) {
             const int st = c % STAGES;
             const unsigned ph = (c / STAGES) & 1;
             if (dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
@@ -362,14 +382,14 @@ cudaError_t launch_p(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensor
     int dev = 0, sms = 0, per_sm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Geo<D, CW>::kThreads, smem)) != cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, persistent_threads<D, CW>(), smem)) != cudaSuccess)
         return e;
     plan_kernel<T, D><<<1, kPlanThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.head_groups * a.max_parts * a.num_seqs;
     int64_t grid = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
     if (grid > units) grid = units;
-    kern<<<static_cast<unsigned>(grid), Geo<D, CW>::kThreads, smem, s>>>(tmk, tmv, a);
+    kern<<<static_cast<unsigned>(grid), persistent_threads<D, CW>(), smem, s>>>(tmk, tmv, a);
     return cudaGetLastError();
 }
 

@@ -96,6 +96,15 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy (completion tracked per thread by
+// commit groups: cp_async_commit / cp_async_wait_all).
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Contiguous global -> shared bulk copy (16-byte aligned addresses, size a
 // multiple of 16), completion counted on `bar` (bytes).
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
