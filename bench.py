@@ -47,9 +47,12 @@ def parse_args():
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    p.add_argument("--op", default="decode", choices=["decode", "swap"],
+                   help="decode: the decode step (default); swap: preemption swap-out/in of a quarter of the batch")
     p.add_argument("--workload", default="llama3_8b", choices=sorted(W.SPECS))
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
+    p.add_argument("--ref-seconds", type=float, default=90.0, help="total budget of the --impl reference run")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -397,7 +400,7 @@ def run_reference(args, rank, world):
     pools = W.host_pools_for(wl, seqs, 0)
     # size each step: time one sequence, then give each step ~budget/(K+W)
     b1, s1, _ = time_oracle(wl, [np.array(x, copy=True) for x in pools], seqs[:1], 0.0)
-    per_step_s = min(5.0, max(s1, 90.0 / max(1, args.steps + args.warmup)))
+    per_step_s = min(5.0, max(s1, args.ref_seconds / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(wl, pools, seqs, per_step_s)
     tot_b, tot_s, tot_n = 0, 0.0, 0
@@ -419,11 +422,92 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- swap (preemption) measurement
+def run_swap(args, rank, world, local):
+    """Swap a quarter of the batch's sequences out to pinned host pools and back in.
+
+    One step = swap-out (device -> pinned host) then swap-in (host -> device,
+    new block ids) of every block those sequences use, all layers.  Bytes are
+    the K and V bytes of the swapped blocks, counted once per direction.
+    """
+    from paged_kv_cache_156_gb300 import _build
+
+    if local == 0:
+        _build.build()
+    barrier(world)
+    import paged_kv_cache_156_gb300 as pkv
+
+    pkv.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = W.SPECS[args.workload]
+    wl = W.build(spec, values="none")
+    tdt = torch.float16 if spec.dtype == W.F16 else torch.bfloat16
+    bs = spec.block_size
+    seqs = list(range(0, spec.num_seqs, 4))
+    used = np.unique(np.concatenate([wl.block_tables[s, :W.blocks_needed(int(wl.seq_lens[s]), bs)] for s in seqs]))
+    nb = len(used)
+    layers = spec.num_layers
+    kcs, vcs = [], []
+    for l in range(layers):
+        k, v = W.device_pools(wl, l, dev)
+        kcs.append(k)
+        vcs.append(v)
+    shape = (nb,) + tuple(kcs[0].shape[1:])
+    hk = [torch.empty(shape, dtype=tdt, pin_memory=True) for _ in range(layers)]
+    hv = [torch.empty(shape, dtype=tdt, pin_memory=True) for _ in range(layers)]
+    free = np.setdiff1d(np.arange(wl.num_blocks), used)
+    back = np.concatenate([free, used])[:nb]
+    out_pairs = torch.from_numpy(np.stack([used, np.arange(nb)], 1).astype(np.int64)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(nb), back], 1).astype(np.int64)).to(dev)
+    block_bytes = 2 * bs * spec.num_kv_heads * spec.head_dim * 2 * layers     # K and V, all layers
+    ev = []
+
+    def step(timed):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record()
+        pkv.swap_blocks(kcs, vcs, hk, hv, out_pairs)
+        b.record()
+        pkv.swap_blocks(hk, hv, kcs, vcs, in_pairs)
+        c.record()
+        if timed:
+            ev.append((a, b, c))
+
+    for _ in range(max(3, args.warmup)):
+        step(False)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step(True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    assert pkv.device_error() == 0
+    out_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
+    in_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev]))
+    step_bytes = 2 * nb * block_bytes
+    if rank != 0:
+        return None
+    return {"metric": "swap_blocks: device <-> pinned host GB/s (swap-out then swap-in)",
+            "value": round(world * step_bytes * args.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+            "data": "synthetic", "config": {"workload": spec.name, "swapped_sequences": len(seqs), "blocks": int(nb),
+                                            "bytes_per_direction": int(nb * block_bytes), "layers": layers},
+            "swap_out_GBps": round(nb * block_bytes / (out_ms / 1e3) / 1e9, 2),
+            "swap_in_GBps": round(nb * block_bytes / (in_ms / 1e3) / 1e9, 2),
+            "gpu_launches": 2 * args.steps * ((layers + 63) // 64)}
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.op == "swap":
+        res = run_swap(args, rank, world, local)
     else:
         res = run_pkv(args, rank, world, local)
     if rank == 0 and res is not None:

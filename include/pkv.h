@@ -166,6 +166,32 @@ PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_c
                            int block_size, int num_kv_heads, int head_dim, pkv_dtype dt, void* stream);
 
 /*
+ * swap_blocks -- move blocks between the device pool and a host pool
+ * (preemption by swapping).
+ *
+ * P2 §3.1 (the scheduler output's blocks_to_swap_in / blocks_to_swap_out) and
+ * §3.2 (Swapping: a preempted request's blocks are copied from GPU memory to
+ * CPU memory, freeing the GPU blocks, and copied back when it resumes); P1
+ * §4.2.4 (--swap-space).  For every pair i and every layer l:
+ *     dst_key_caches[l][dst_i] = src_key_caches[l][src_i], and the same for V,
+ * bit for bit, where (src_i, dst_i) = src_dst_pairs[i].
+ *
+ *   src_*_caches, dst_*_caches  HOST arrays of num_layers pointers, each a pool
+ *                 [num_blocks][block_size][num_kv_heads][head_dim] that the GPU
+ *                 can address: device memory, or pinned host memory (cudaHostAlloc,
+ *                 or torch pin_memory; pinned memory is mapped under unified
+ *                 addressing).  Swap-out: device -> host; swap-in: host -> device.
+ *   src_dst_pairs DEVICE int64 [num_pairs][2]; a source block id in
+ *                 [0, src_num_blocks), a destination id in [0, dst_num_blocks)
+ * Destinations must be distinct.  num_pairs == 0 or num_layers == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_swap_blocks(void* const* src_key_caches, void* const* src_value_caches,
+                           void* const* dst_key_caches, void* const* dst_value_caches, int num_layers,
+                           const int64_t* src_dst_pairs, int64_t num_pairs, int64_t src_num_blocks,
+                           int64_t dst_num_blocks, int block_size, int num_kv_heads, int head_dim,
+                           pkv_dtype dt, void* stream);
+
+/*
  * Device error word: bit 0 = a block id or slot out of range was skipped,
  * bit 1 = a pipeline wait gave up after its time limit.  Reads the word of
  * the current device after synchronising it, stores it in *value and, if

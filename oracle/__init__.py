@@ -126,6 +126,19 @@ def copy_blocks_ref(key_caches, value_caches, pairs) -> None:
             vc[dst] = vc[src]
 
 
+def swap_blocks_ref(src_key_caches, src_value_caches, dst_key_caches, dst_value_caches, pairs) -> None:
+    """Preemption swap: for each (src, dst), dst_cache[dst] = src_cache[src], every layer.
+
+    P2 §3.1 (``blocks_to_swap_in`` / ``blocks_to_swap_out``) and §3.2 (a
+    preempted request's blocks are copied to CPU memory and back).  The two
+    pools may differ in size; a block keeps its contents, only its id changes.
+    """
+    for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist():
+        for sk, sv, dk, dv in zip(src_key_caches, src_value_caches, dst_key_caches, dst_value_caches):
+            dk[dst] = sk[src]
+            dv[dst] = sv[src]
+
+
 # --------------------------------------------------------------------------
 # attention (P4 §2.2 paged_attention_kernel, read per the module docstring)
 # --------------------------------------------------------------------------

@@ -26,7 +26,7 @@ _DT = {torch.float16: 0, torch.bfloat16: 1}
 # every symbol include/pkv.h declares
 ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
                "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
-               "pkv_paged_attention_decode_static")
+               "pkv_paged_attention_decode_static", "pkv_swap_blocks")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load() -> ctypes.CDLL:
                                     c_i, c_i, c_p]
     lib.pkv_device_error.restype = c_i
     lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), c_i]
+    lib.pkv_swap_blocks.restype = c_i
+    lib.pkv_swap_blocks.argtypes = [ctypes.POINTER(c_p)] * 4 + [c_i, c_p, c_i64, c_i64, c_i64, c_i, c_i, c_i, c_i, c_p]
     lib.pkv_paged_attention_decode_static.restype = c_i
     lib.pkv_paged_attention_decode_static.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                       c_i64, c_f, c_i, c_i, c_p]
@@ -185,6 +187,44 @@ def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:
     NB, bs, Hkv, d = shape
     _check(load().pkv_copy_blocks(karr, varr, n, ctypes.c_void_p(src_dst_pairs.data_ptr()), src_dst_pairs.shape[0],
                                   NB, bs, Hkv, d, _DT[dt], _stream(key_caches[0])))
+
+
+def _addressable_pool(name, t):
+    """A pool the GPU can address: a CUDA tensor or a pinned CPU tensor."""
+    if not isinstance(t, torch.Tensor) or t.dim() != 4 or t.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError(f"{name} must be a 4-D fp16/bf16 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    return t.data_ptr()
+
+
+def swap_blocks(src_key_caches, src_value_caches, dst_key_caches, dst_value_caches, src_dst_pairs) -> None:
+    """dst[dst_i] = src[src_i] for every (src_i, dst_i) row of src_dst_pairs (int64 [Np, 2], on the GPU),
+    for every layer's K and V pool.  Pools are CUDA tensors or pinned host tensors (swap out / swap in)."""
+    lists = [src_key_caches, src_value_caches, dst_key_caches, dst_value_caches]
+    lists = [[x] if isinstance(x, torch.Tensor) else list(x) for x in lists]
+    n = len(lists[0])
+    if n == 0 or any(len(x) != n for x in lists):
+        raise ValueError("need the same non-zero number of pools in every list")
+    src_shape, dst_shape, dt = lists[0][0].shape, lists[2][0].shape, lists[0][0].dtype
+    ptrs = []
+    for li, (name, pools) in enumerate(zip(("src_key", "src_value", "dst_key", "dst_value"), lists)):
+        want = src_shape if li < 2 else dst_shape
+        for i, t in enumerate(pools):
+            ptrs.append(_addressable_pool(f"{name}[{i}]", t))
+            if t.shape != want or t.dtype != dt:
+                raise ValueError("pools must share dtype; source pools one shape, destination pools another")
+    if tuple(src_shape[1:]) != tuple(dst_shape[1:]):
+        raise ValueError("source and destination blocks must have the same shape")
+    _cuda("src_dst_pairs", src_dst_pairs, torch.int64, 2)
+    if src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [Np, 2]")
+    arrs = [(ctypes.c_void_p * n)(*ptrs[k * n:(k + 1) * n]) for k in range(4)]
+    _, bs, Hkv, d = src_shape
+    _check(load().pkv_swap_blocks(*arrs, n, ctypes.c_void_p(src_dst_pairs.data_ptr()), src_dst_pairs.shape[0],
+                                  src_shape[0], dst_shape[0], bs, Hkv, d, _DT[dt], _stream(src_dst_pairs)))
 
 
 def device_error(reset: bool = True) -> int:

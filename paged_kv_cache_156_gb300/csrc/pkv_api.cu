@@ -298,39 +298,74 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     return ok();
 }
 
-pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
-                           const int64_t* src_dst_pairs, int64_t num_pairs, int64_t num_blocks, int block_size,
-                           int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
-    if (num_layers < 0 || num_pairs < 0) return fail(PKV_ERR_INVALID, "num_layers / num_pairs < 0");
-    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
-    if (block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
-        return fail(PKV_ERR_INVALID, "bad pool shape");
+}  // extern "C"
+
+namespace {
+
+// Shared by copy_blocks (one pool) and swap_blocks (two pools).
+pkv_status block_copies(void* const* src_key, void* const* src_value, void* const* dst_key, void* const* dst_value,
+                        int num_layers, const int64_t* src_dst_pairs, int64_t num_pairs, int64_t src_num_blocks,
+                        int64_t dst_num_blocks, int block_size, int num_kv_heads, int head_dim, pkv_dtype dt,
+                        void* stream, const char* what) {
+    if (num_layers < 0 || num_pairs < 0) return fail(PKV_ERR_INVALID, "%s: num_layers / num_pairs < 0", what);
+    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "%s: dtype %d", what, static_cast<int>(dt));
+    if (block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return fail(PKV_ERR_INVALID, "%s: bad pool shape", what);
     const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
-    if (block_bytes % 16 != 0) return fail(PKV_ERR_INVALID, "block bytes %lld not a multiple of 16", static_cast<long long>(block_bytes));
+    if (block_bytes % 16 != 0)
+        return fail(PKV_ERR_INVALID, "%s: block bytes %lld not a multiple of 16", what,
+                    static_cast<long long>(block_bytes));
     if (num_layers == 0 || num_pairs == 0) return ok();
-    if (!key_caches || !value_caches || !src_dst_pairs) return fail(PKV_ERR_INVALID, "null pointer");
-    if (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) return fail(PKV_ERR_INVALID, "pairs must be 8-byte aligned");
-    for (int l = 0; l < num_layers; ++l)
-        if (!key_caches[l] || !value_caches[l] || !aligned16(key_caches[l]) || !aligned16(value_caches[l]))
-            return fail(PKV_ERR_INVALID, "layer %d cache pointer null or not 16-byte aligned", l);
+    if (!src_key || !src_value || !dst_key || !dst_value || !src_dst_pairs)
+        return fail(PKV_ERR_INVALID, "%s: null pointer", what);
+    if (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) return fail(PKV_ERR_INVALID, "%s: pairs must be 8-byte aligned", what);
+    for (int l = 0; l < num_layers; ++l) {
+        const void* p[4] = {src_key[l], src_value[l], dst_key[l], dst_value[l]};
+        for (const void* x : p)
+            if (!x || !aligned16(x))
+                return fail(PKV_ERR_INVALID, "%s: layer %d pool pointer null or not 16-byte aligned", what, l);
+    }
     const int dev = current_device();
     for (int l0 = 0; l0 < num_layers; l0 += pkv::kMaxCopyLayers) {
         pkv::CopyArgs a;
         const int n = num_layers - l0 < pkv::kMaxCopyLayers ? num_layers - l0 : pkv::kMaxCopyLayers;
         for (int i = 0; i < pkv::kMaxCopyLayers; ++i) {
-            a.key[i] = i < n ? static_cast<uint4*>(key_caches[l0 + i]) : nullptr;
-            a.value[i] = i < n ? static_cast<uint4*>(value_caches[l0 + i]) : nullptr;
+            a.src_key[i] = i < n ? static_cast<const uint4*>(src_key[l0 + i]) : nullptr;
+            a.src_value[i] = i < n ? static_cast<const uint4*>(src_value[l0 + i]) : nullptr;
+            a.dst_key[i] = i < n ? static_cast<uint4*>(dst_key[l0 + i]) : nullptr;
+            a.dst_value[i] = i < n ? static_cast<uint4*>(dst_value[l0 + i]) : nullptr;
         }
         a.pairs = src_dst_pairs;
         a.num_pairs = num_pairs;
-        a.num_blocks = num_blocks;
+        a.src_num_blocks = src_num_blocks;
+        a.dst_num_blocks = dst_num_blocks;
         a.num_layers = n;
         a.block_vecs = static_cast<int>(block_bytes / 16);
         a.err = error_word(dev);
         cudaError_t e = pkv::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "copy_blocks launch: %s", cudaGetErrorString(e));
+        if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
     }
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                           const int64_t* src_dst_pairs, int64_t num_pairs, int64_t num_blocks, int block_size,
+                           int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    return block_copies(key_caches, value_caches, key_caches, value_caches, num_layers, src_dst_pairs, num_pairs,
+                        num_blocks, num_blocks, block_size, num_kv_heads, head_dim, dt, stream, "copy_blocks");
+}
+
+pkv_status pkv_swap_blocks(void* const* src_key_caches, void* const* src_value_caches, void* const* dst_key_caches,
+                           void* const* dst_value_caches, int num_layers, const int64_t* src_dst_pairs,
+                           int64_t num_pairs, int64_t src_num_blocks, int64_t dst_num_blocks, int block_size,
+                           int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    return block_copies(src_key_caches, src_value_caches, dst_key_caches, dst_value_caches, num_layers, src_dst_pairs,
+                        num_pairs, src_num_blocks, dst_num_blocks, block_size, num_kv_heads, head_dim, dt, stream,
+                        "swap_blocks");
 }
 
 pkv_status pkv_device_error(unsigned int* value, int reset) {

@@ -1,11 +1,16 @@
-// copy_blocks: the copy-on-write block copy issued at a fork.
+// Block copies: the copy-on-write copy issued at a fork, and the swap of
+// blocks between the device pool and a pinned host pool.
 //
-// "LLM 推理引擎内部原理" §3.1 / §3.3 (blocks_to_copy, Copy-on-Write) and
-// "vLLM核心概念" §4.2.2: before a sequence writes into a block it shares, the
-// block is copied to a private one.  A physical block of one layer's pool is
+// "LLM 推理引擎内部原理" §3.1 (the scheduler output's blocks_to_copy,
+// blocks_to_swap_in, blocks_to_swap_out), §3.2 (preemption by swapping:
+// blocks move to CPU memory and back) and §3.3 (Copy-on-Write); "vLLM核心概念"
+// §4.2.2: before a sequence writes into a block it shares, the block is
+// copied to a private one.  A physical block of one layer's pool is
 // block_size * num_kv_heads * head_dim contiguous elements, so each (pair,
-// layer) is two contiguous memcpy's of that size (K and V), done here with
-// 16-byte vector loads spread over several CTAs per block.
+// layer) is two contiguous copies of that size (K and V), done with 16-byte
+// vector loads spread over several CTAs per block.  Pinned host memory is
+// addressed directly by the kernel (unified addressing), so a swap is the
+// same gather as a copy.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -16,15 +21,15 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) copy_blocks_kernel(const CopyArgs a) {
     const int layer = blockIdx.z;
-    const uint4* kbase = a.key[layer];
-    const uint4* vbase = a.value[layer];
-    uint4* kout = a.key[layer];
-    uint4* vout = a.value[layer];
+    const uint4* kbase = a.src_key[layer];
+    const uint4* vbase = a.src_value[layer];
+    uint4* kout = a.dst_key[layer];
+    uint4* vout = a.dst_value[layer];
     const int64_t bv = a.block_vecs;
     for (int64_t i = blockIdx.y; i < a.num_pairs; i += gridDim.y) {
         const int64_t src = a.pairs[2 * i];
         const int64_t dst = a.pairs[2 * i + 1];
-        if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+        if (src < 0 || src >= a.src_num_blocks || dst < 0 || dst >= a.dst_num_blocks) {
             if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.err, kErrBounds);
             continue;
         }

@@ -22,12 +22,17 @@ struct AppendArgs {
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 
+// Block copies between two pools of the same block shape (the same pool for
+// copy-on-write, a device pool and a pinned host pool for swapping).
 struct CopyArgs {
-    uint4* key[kMaxCopyLayers];
-    uint4* value[kMaxCopyLayers];
-    const int64_t* pairs;    // [num_pairs][2]
+    const uint4* src_key[kMaxCopyLayers];
+    const uint4* src_value[kMaxCopyLayers];
+    uint4* dst_key[kMaxCopyLayers];
+    uint4* dst_value[kMaxCopyLayers];
+    const int64_t* pairs;    // [num_pairs][2] (source block, destination block)
     int64_t num_pairs;
-    int64_t num_blocks;
+    int64_t src_num_blocks;
+    int64_t dst_num_blocks;
     int num_layers;
     int block_vecs;          // block_size * num_kv_heads * head_dim * 2 / 16
     unsigned* err;

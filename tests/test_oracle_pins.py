@@ -201,6 +201,28 @@ def test_copy_blocks_ref_cow_example():
         assert np.array_equal(k1[untouched], k0[untouched]) and np.array_equal(v1[untouched], v0[untouched])
 
 
+def test_swap_round_trip_preserves_attention():
+    """Swapping a sequence's blocks out to a host pool and back in under new ids
+    (P2 §3.2) leaves its attention unchanged once its table names the new ids."""
+    rng = np.random.default_rng(13)
+    NB, bs, Hkv, d, L = 20, 8, 2, 16, 37
+    kc, vc = _rand_pool(rng, NB, bs, Hkv, d)
+    table = np.array([3, 17, 0, 11, 5], dtype=np.int64)
+    q = bits(rng.standard_normal((1, 4, d)))
+    before = oracle.attention_ref(q, kc, vc, table[None], np.array([L]), 0.25, Hkv, F16)
+    host_k = np.zeros((8, bs, Hkv, d), np.uint16)
+    host_v = np.zeros((8, bs, Hkv, d), np.uint16)
+    out_pairs = np.stack([table, np.arange(5)], axis=1)
+    oracle.swap_blocks_ref([kc], [vc], [host_k], [host_v], out_pairs)
+    assert all(np.array_equal(host_k[j], kc[b]) for j, b in enumerate(table))
+    kc2 = np.full_like(kc, NAN_BITS[F16])
+    vc2 = np.full_like(vc, NAN_BITS[F16])
+    new_ids = np.array([9, 2, 14, 19, 6], dtype=np.int64)
+    oracle.swap_blocks_ref([host_k], [host_v], [kc2], [vc2], np.stack([np.arange(5), new_ids], axis=1))
+    after = oracle.attention_ref(q, kc2, vc2, new_ids[None], np.array([L]), 0.25, Hkv, F16)
+    assert np.array_equal(before, after)
+
+
 # ---------------------------------------------------------------- attention
 def att_contig(q, K, V, scale, bs=16, dtype=F16, perm=None):
     """Oracle attention for one sequence with one KV head given float K/V [L, d]."""
