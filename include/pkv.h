@@ -55,7 +55,8 @@ typedef enum {
     PKV_ERR_INVALID = 1,      /* bad pointer, size, shape or alignment               */
     PKV_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, block_size, dtype    */
     PKV_ERR_WORKSPACE = 3,    /* decode workspace missing or too small               */
-    PKV_ERR_CUDA = 4          /* a CUDA runtime call or launch failed                */
+    PKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed                */
+    PKV_ERR_OOM = 5           /* block manager: not enough free blocks (nothing changed) */
 } pkv_status;
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -234,6 +235,57 @@ PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* q, c
                                       int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
                                       int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
                                       int partition_tokens, void* stream);
+
+/*
+ * Host block manager (host memory only; no GPU call).
+ *
+ * P2 §2.3 (BlockEngine: free blocks in a FIFO list; allocate takes
+ * ceil(num_tokens / block_size) blocks from its front; append_slot gives the
+ * slot of a sequence's next token, taking a new block when the last one is
+ * full, or reports exhaustion so the scheduler can preempt; free returns the
+ * blocks to the back of the list) and §3.3 (forked samples share prefix
+ * blocks); P1 §4.2.2 (a writer to a shared block copies it first); P4 §五
+ * (shared blocks are reference counted and not freed while shared).
+ *
+ * One manager per pool; not thread-safe.  Every call checks before it changes
+ * anything: PKV_ERR_OOM and PKV_ERR_INVALID leave the manager as it was.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of blocks 0..num_blocks-1; `free_order` (host, optional) is the
+ * initial order of the free list (a permutation of the pool), NULL = 0, 1, ...
+ * Returns NULL on bad arguments or allocation failure. */
+PKV_API pkv_block_manager* pkv_bm_create(int64_t num_blocks, int block_size, const int64_t* free_order);
+PKV_API void pkv_bm_destroy(pkv_block_manager* bm);
+PKV_API int64_t pkv_bm_num_free_blocks(const pkv_block_manager* bm);
+/* Tokens held by a sequence, or -1 if the id is unknown. */
+PKV_API int64_t pkv_bm_seq_len(const pkv_block_manager* bm, int64_t seq_id);
+/* Sequences sharing a block (0 = free), or -1 for an id outside the pool. */
+PKV_API int pkv_bm_refcount(const pkv_block_manager* bm, int64_t block);
+
+/* A new sequence holding num_tokens tokens (its prompt) in fresh blocks. */
+PKV_API pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq_id, int64_t num_tokens);
+/* child_id shares every block of parent_id (parallel sampling, beam search). */
+PKV_API pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id);
+/* Drop a sequence; blocks no other sequence holds go back to the free list. */
+PKV_API pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
+
+/*
+ * One new token for each of n distinct sequences.  slots[i] receives the flat
+ * slot (physical_block * block_size + offset) of seq_ids[i]'s new token.  A
+ * sequence whose last block is partly filled and shared gets a private copy
+ * first: (shared block, new block) is appended to cow_pairs (host int64
+ * [cow_capacity][2]) and *num_cow counts the pairs, to be passed to
+ * pkv_copy_blocks before the slot writes.  PKV_ERR_OOM if the free list cannot
+ * cover every sequence of the call.
+ */
+PKV_API pkv_status pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int64_t n, int64_t* slots,
+                                       int64_t* cow_pairs, int64_t cow_capacity, int64_t* num_cow);
+
+/* Block tables (host int32 [n][max_blocks_per_seq], rows padded with `pad`)
+ * and lengths (host int32 [n]) of n sequences, the decode call's inputs. */
+PKV_API pkv_status pkv_bm_block_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int64_t n,
+                                       int32_t* tables, int max_blocks_per_seq, int32_t pad, int32_t* seq_lens);
 
 #ifdef __cplusplus
 }

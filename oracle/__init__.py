@@ -249,3 +249,90 @@ def decode_step_ref(key_caches, value_caches, copy_pairs, k_new, v_new, slot_map
             outs[l] = attention_ref(ql, kcs[l], vcs[l], block_tables, seq_lens, scale,
                                     num_kv_heads, dtype)
     return outs, kcs, vcs
+
+
+# --------------------------------------------------------------------------
+# host block manager (P2 §2.3 BlockEngine, §3.3; P1 §4.2.2; P4 §五)
+# --------------------------------------------------------------------------
+class BlockEngineRef:
+    """Plain reference of the host block manager.
+
+    P2 §2.3: the free blocks form a FIFO list; ``allocate`` takes
+    ceil(tokens / block_size) blocks from its front; the next token of a
+    sequence goes to ``blocks[-1] * bs + len % bs`` unless the last block is
+    full (``len % bs == 0``), in which case a block is taken from the front;
+    an empty list means "no slot" (the scheduler must preempt); ``free``
+    returns blocks to the back.  P2 §3.3 / P4 §五: a fork shares the parent's
+    blocks, each block counting its holders, and a block is only returned when
+    no sequence holds it.  P1 §4.2.2: a sequence about to write into a block
+    that another sequence also holds first copies it into a block of its own.
+    Calls that cannot complete change nothing and return False.
+    """
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        from collections import deque
+
+        self.bs = block_size
+        self.free_list = deque(range(num_blocks) if free_order is None else [int(b) for b in free_order])
+        self.ref = [0] * num_blocks
+        self.tables = {}
+        self.lens = {}
+
+    def allocate(self, seq_id, num_tokens):
+        if seq_id in self.tables or num_tokens < 0:
+            return False
+        n = num_logical_blocks(num_tokens, self.bs)
+        if n > len(self.free_list):
+            return False
+        blocks = [self.free_list.popleft() for _ in range(n)]
+        for b in blocks:
+            self.ref[b] = 1
+        self.tables[seq_id] = blocks
+        self.lens[seq_id] = num_tokens
+        return True
+
+    def fork(self, parent, child):
+        if parent not in self.tables or child in self.tables:
+            return False
+        self.tables[child] = list(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+        for b in self.tables[child]:
+            self.ref[b] += 1
+        return True
+
+    def free(self, seq_id):
+        if seq_id not in self.tables:
+            return False
+        for b in self.tables.pop(seq_id):
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free_list.append(b)
+        del self.lens[seq_id]
+        return True
+
+    def _needs_block(self, s):
+        L = self.lens[s]
+        return L % self.bs == 0 or self.ref[self.tables[s][-1]] > 1
+
+    def append_slots(self, seq_ids):
+        """One token for each sequence; (slots, copy-on-write pairs) or None."""
+        if len(set(seq_ids)) != len(seq_ids) or any(s not in self.tables for s in seq_ids):
+            return None
+        if sum(self._needs_block(s) for s in seq_ids) > len(self.free_list):
+            return None
+        slots, pairs = [], []
+        for s in seq_ids:
+            L, t = self.lens[s], self.tables[s]
+            if L % self.bs == 0:
+                b = self.free_list.popleft()
+                self.ref[b] = 1
+                t.append(b)
+            elif self.ref[t[-1]] > 1:
+                b = self.free_list.popleft()
+                self.ref[b] = 1
+                self.ref[t[-1]] -= 1
+                pairs.append((t[-1], b))
+                t[-1] = b
+            slots.append(slot_for_position(t, L, self.bs))
+            self.lens[s] = L + 1
+        return slots, pairs

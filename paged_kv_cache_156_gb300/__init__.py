@@ -20,13 +20,15 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
 
-PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_OOM = range(6)
 _DT = {torch.float16: 0, torch.bfloat16: 1}
 
 # every symbol include/pkv.h declares
 ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
                "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
-               "pkv_paged_attention_decode_static", "pkv_swap_blocks")
+               "pkv_paged_attention_decode_static", "pkv_swap_blocks", "pkv_bm_create", "pkv_bm_destroy",
+               "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
+               "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables")
 
 _lib = None
 
@@ -66,6 +68,22 @@ def load() -> ctypes.CDLL:
     lib.pkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), c_i]
     lib.pkv_swap_blocks.restype = c_i
     lib.pkv_swap_blocks.argtypes = [ctypes.POINTER(c_p)] * 4 + [c_i, c_p, c_i64, c_i64, c_i64, c_i, c_i, c_i, c_i, c_p]
+    lib.pkv_bm_create.restype = c_p
+    lib.pkv_bm_create.argtypes = [c_i64, c_i, c_p]
+    lib.pkv_bm_destroy.restype = None
+    lib.pkv_bm_destroy.argtypes = [c_p]
+    lib.pkv_bm_num_free_blocks.restype = c_i64
+    lib.pkv_bm_num_free_blocks.argtypes = [c_p]
+    lib.pkv_bm_seq_len.restype = c_i64
+    lib.pkv_bm_seq_len.argtypes = [c_p, c_i64]
+    lib.pkv_bm_refcount.restype = c_i
+    lib.pkv_bm_refcount.argtypes = [c_p, c_i64]
+    for name, args in (("pkv_bm_allocate", [c_p, c_i64, c_i64]), ("pkv_bm_fork", [c_p, c_i64, c_i64]),
+                       ("pkv_bm_free", [c_p, c_i64]),
+                       ("pkv_bm_append_slots", [c_p, c_p, c_i64, c_p, c_p, c_i64, c_p]),
+                       ("pkv_bm_block_tables", [c_p, c_p, c_i64, c_p, c_i, ctypes.c_int32, c_p])):
+        getattr(lib, name).restype = c_i
+        getattr(lib, name).argtypes = args
     lib.pkv_paged_attention_decode_static.restype = c_i
     lib.pkv_paged_attention_decode_static.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                       c_i64, c_f, c_i, c_i, c_p]
@@ -225,6 +243,69 @@ def swap_blocks(src_key_caches, src_value_caches, dst_key_caches, dst_value_cach
     _, bs, Hkv, d = src_shape
     _check(load().pkv_swap_blocks(*arrs, n, ctypes.c_void_p(src_dst_pairs.data_ptr()), src_dst_pairs.shape[0],
                                   src_shape[0], dst_shape[0], bs, Hkv, d, _DT[dt], _stream(src_dst_pairs)))
+
+
+class BlockManager:
+    """The library's host block manager (``pkv_bm_*``): free list, reference
+    counts, copy-on-write at a fork.  Host only; it produces the inputs of the
+    decode step (tables, lengths, slots) and the copy pairs for copy_blocks."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        import numpy as np
+
+        self._np = np
+        self.block_size = int(block_size)
+        self._order = None if free_order is None else np.ascontiguousarray(free_order, dtype=np.int64)
+        ptr = None if self._order is None else self._order.ctypes.data
+        self._h = load().pkv_bm_create(int(num_blocks), self.block_size, ptr)
+        if not self._h:
+            raise ValueError("bad block manager arguments")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            load().pkv_bm_destroy(h)
+            self._h = None
+
+    @property
+    def num_free_blocks(self) -> int:
+        return int(load().pkv_bm_num_free_blocks(self._h))
+
+    def seq_len(self, seq_id) -> int:
+        return int(load().pkv_bm_seq_len(self._h, int(seq_id)))
+
+    def refcount(self, block) -> int:
+        return int(load().pkv_bm_refcount(self._h, int(block)))
+
+    def allocate(self, seq_id, num_tokens) -> None:
+        _check(load().pkv_bm_allocate(self._h, int(seq_id), int(num_tokens)))
+
+    def fork(self, parent_id, child_id) -> None:
+        _check(load().pkv_bm_fork(self._h, int(parent_id), int(child_id)))
+
+    def free(self, seq_id) -> None:
+        _check(load().pkv_bm_free(self._h, int(seq_id)))
+
+    def append_slots(self, seq_ids):
+        """One new token per sequence: (slots int64 [n], cow_pairs int64 [k, 2])."""
+        np = self._np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        slots = np.empty(len(ids), dtype=np.int64)
+        cow = np.empty((max(1, len(ids)), 2), dtype=np.int64)
+        n = ctypes.c_int64(0)
+        _check(load().pkv_bm_append_slots(self._h, ids.ctypes.data, len(ids), slots.ctypes.data, cow.ctypes.data,
+                                          cow.shape[0], ctypes.byref(n)))
+        return slots, cow[:n.value].copy()
+
+    def block_tables(self, seq_ids, max_blocks_per_seq, pad=-1):
+        """(int32 [n, max_blocks_per_seq] tables padded with `pad`, int32 [n] lengths)."""
+        np = self._np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tables = np.empty((len(ids), max_blocks_per_seq), dtype=np.int32)
+        lens = np.empty(len(ids), dtype=np.int32)
+        _check(load().pkv_bm_block_tables(self._h, ids.ctypes.data, len(ids), tables.ctypes.data,
+                                          int(max_blocks_per_seq), int(pad), lens.ctypes.data))
+        return tables, lens
 
 
 def device_error(reset: bool = True) -> int:

@@ -1,6 +1,6 @@
 """Build the CUDA library ``_lib/libpkv.so`` in-tree with nvcc (sm_103a only).
 
-Each ``csrc/*.cu`` file is compiled to an object in parallel, then linked into
+Each ``csrc/*.cu`` / ``csrc/*.cpp`` file is compiled to an object in parallel, then linked into
 one shared library with the CUDA runtime linked statically, so the library
 loads on a machine without a GPU (the symbol checks run there) and carries no
 dependency beyond the driver at run time.
@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
