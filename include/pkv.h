@@ -148,6 +148,34 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, const vo
                                       void* stream);
 
 /*
+ * paged_attention_verify -- num_queries query tokens per sequence over its
+ * paged K/V, causal among themselves (the verification step of speculative
+ * decoding).
+ *
+ * P1 §4.4.2 (the target model takes the K draft tokens as input and computes
+ * their distributions in one forward pass); P3 §4.2 (speculative_verify:
+ * the large model scores all gamma candidates in one pass over the prefix KV);
+ * P2 §5.2 (the candidates' KV lives in the same block structure).  The last
+ * num_queries positions of sequence s hold the query tokens' own K/V (written
+ * by pkv_paged_kv_append first); query token i (0-based) attends over
+ * positions t < seq_lens[s] - num_queries + i + 1, otherwise exactly as
+ * pkv_paged_attention_decode.  num_queries = 1 is the decode call.
+ *
+ *   out, q        [num_seqs][num_queries][num_heads][head_dim]
+ *   workspace     pkv_decode_workspace_bytes(num_seqs, num_heads * num_queries,
+ *                 num_kv_heads, head_dim, max_seq_len, partition_tokens) bytes
+ *   num_queries   in [1, 64]; seq_lens[s] should be 0 or >= num_queries (a
+ *                 query token that sees no position gets a zero output)
+ */
+PKV_API pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                      int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                      int num_queries, void* workspace, size_t workspace_bytes,
+                                      int partition_tokens, void* stream);
+
+/*
  * copy_blocks -- the copy-on-write block copy at a fork.
  *
  * P2 §3.1 (the scheduler output's blocks_to_copy, "用于 Copy-on-Write") and

@@ -197,6 +197,34 @@ def attention_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
     return out
 
 
+def verify_attention_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                         block_tables: np.ndarray, seq_lens: np.ndarray, scale: float, num_kv_heads: int,
+                         dtype: str) -> np.ndarray:
+    """Multi-query paged attention; float64 [B, nq, num_heads, head_dim].
+
+    q: uint16 bits [B, nq, Hq, d].  The last nq positions of sequence s are the
+    query tokens' own (P1 §4.4.2: the target model scores all draft tokens in
+    one pass; P3 §4.2 speculative_verify).  Query token i sees the prefix and
+    the query tokens before it and itself, i.e. positions t < L_s - nq + i + 1
+    (causal).  A query that sees no position gets zeros.
+    """
+    B, nq, Hq, d = q.shape
+    G = Hq // num_kv_heads
+    out = np.zeros((B, nq, Hq, d), dtype=np.float64)
+    for s in range(B):
+        L = int(seq_lens[s])
+        for g in range(num_kv_heads):
+            K = gather_sequence(key_cache, block_tables[s], L, g, dtype)
+            V = gather_sequence(value_cache, block_tables[s], L, g, dtype)
+            for i in range(nq):
+                vis = L - nq + i + 1
+                if L <= 0 or vis <= 0:
+                    continue
+                for h in range(g * G, (g + 1) * G):
+                    out[s, i, h] = softmax_attention(decode_bits(q[s, i, h], dtype), K[:vis], V[:vis], scale)
+    return out
+
+
 # --------------------------------------------------------------------------
 # split-K pieces: partial softmax over a slice of positions and its merge
 # --------------------------------------------------------------------------

@@ -26,7 +26,7 @@ _DT = {torch.float16: 0, torch.bfloat16: 1}
 # every symbol include/pkv.h declares
 ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
                "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
-               "pkv_paged_attention_decode_static", "pkv_swap_blocks", "pkv_bm_create", "pkv_bm_destroy",
+               "pkv_paged_attention_decode_static", "pkv_swap_blocks", "pkv_paged_attention_verify", "pkv_bm_create", "pkv_bm_destroy",
                "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
                "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables")
 
@@ -61,6 +61,9 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode.restype = c_i
     lib.pkv_paged_attention_decode.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_paged_attention_verify.restype = c_i
+    lib.pkv_paged_attention_verify.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
+                                               c_i64, c_f, c_i, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_copy_blocks.restype = c_i
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p, c_i64, c_i64, c_i, c_i,
                                     c_i, c_i, c_p]
@@ -182,6 +185,36 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_len
     _check(load().pkv_paged_attention_decode(
         *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
         NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
+
+
+def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,
+                           workspace=None, partition_tokens=0) -> None:
+    """Multi-query paged attention: q, out [B, nq, Hq, d]; query token i of sequence s attends over
+    positions [0, seq_lens[s] - nq + i] (the last nq positions are the queries' own K/V)."""
+    NB, bs, Hkv, d = _pool("key_cache", key_cache)
+    if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
+        raise ValueError("value_cache must match key_cache")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, num_queries, num_heads, head_dim]")
+    B, nq, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q and out must be [B, num_queries, num_heads, head_dim]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    ptrs = [_cuda("out", out, key_cache.dtype), _cuda("q", q, key_cache.dtype), _cuda("key_cache", key_cache),
+            _cuda("value_cache", value_cache), _cuda("block_tables", block_tables, torch.int32, 2)]
+    _cuda("seq_lens", seq_lens, torch.int32, 1)
+    if block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_tables / seq_lens batch mismatch")
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq * nq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
+    ws_ptr = _cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_attention_verify(
+        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
+        NB, float(scale), _DT[key_cache.dtype], nq, ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
 
 
 def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:

@@ -224,13 +224,21 @@ int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, i
     return resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, 0, head_dim);
 }
 
-pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
-                                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
-                                      int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt, void* workspace,
-                                      size_t workspace_bytes, int partition_tokens, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode (num_queries == 1) and multi-query verify share one path: a KV head
+// serves (num_heads / num_kv_heads) * num_queries query rows.
+pkv_status attention_call(void* out, const void* q, const void* key_cache, const void* value_cache,
+                          const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                          int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                          int64_t num_blocks, float scale, pkv_dtype dt, int num_queries, void* workspace,
+                          size_t workspace_bytes, int partition_tokens, void* stream) {
     pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
     if (st != PKV_OK) return st;
+    if (num_queries < 1 || num_queries > 64) return fail(PKV_ERR_INVALID, "num_queries %d outside [1, 64]", num_queries);
+    const int rows = num_heads * num_queries;            // query rows per sequence
     if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
     if (!valid_block_size(block_size)) return fail(PKV_ERR_UNSUPPORTED, "block_size %d not built (8, 16, 32)", block_size);
     if (num_blocks <= 0 || num_blocks > (int64_t(1) << 31))
@@ -249,18 +257,18 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
         return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned; tables and lengths 4-byte");
 
     const int dev = current_device();
-    const int part = resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, partition_tokens, head_dim);
+    const int part = resolve_partition(num_seqs, rows, num_kv_heads, max_seq_len, partition_tokens, head_dim);
     const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
     if (max_parts > 512)
         return fail(PKV_ERR_UNSUPPORTED, "%lld partitions per sequence (at most 512; use a larger partition_tokens)",
                     static_cast<long long>(max_parts));
     const pkv::DecodeWorkspace lay =
-        pkv::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, static_cast<int>(max_parts));
+        pkv::decode_workspace_layout(num_seqs, rows, num_kv_heads, head_dim, static_cast<int>(max_parts));
     const size_t need = lay.total();
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", need,
                     workspace ? workspace_bytes : size_t(0));
-    const int group = num_heads / num_kv_heads;
+    const int group = rows / num_kv_heads;
     if (static_cast<int64_t>(num_kv_heads) * ((group + 7) / 8) * max_parts * num_seqs >= (int64_t(1) << 31))
         return fail(PKV_ERR_UNSUPPORTED, "too many work items");
 
@@ -287,15 +295,41 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
     a.num_seqs = num_seqs;
     a.num_heads = num_heads;
     a.num_kv_heads = num_kv_heads;
-    a.group = num_heads / num_kv_heads;
+    a.qgroup = num_heads / num_kv_heads;
+    a.num_queries = num_queries;
+    a.group = a.qgroup * num_queries;
     a.head_groups = (a.group + 7) / 8;
     a.block_size = block_size;
     a.part_tokens = part;
     a.max_parts = static_cast<int>(max_parts);
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                      int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt, void* workspace,
+                                      size_t workspace_bytes, int partition_tokens, void* stream) {
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
+                          workspace, workspace_bytes, partition_tokens, stream);
+}
+
+pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_cache, const void* value_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                      int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt, int num_queries,
+                                      void* workspace, size_t workspace_bytes, int partition_tokens, void* stream) {
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt,
+                          num_queries, workspace, workspace_bytes, partition_tokens, stream);
 }
 
 }  // extern "C"

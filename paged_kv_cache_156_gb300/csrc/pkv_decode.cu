@@ -59,7 +59,7 @@ struct Smem {
     static constexpr size_t kBytes = kMisc + 16;
 };
 
-template <typename T, int D, int CW, int STAGES>
+template <typename T, int D, int CW, int STAGES, bool MQ>
 __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                      const __grid_constant__ CUtensorMap tmv,
                                                                      const DecodeArgs a) {
@@ -85,8 +85,9 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     const int s = blockIdx.z;
     const int hg = hh % a.head_groups;
     const int kvh = hh / a.head_groups;
-    const int h0 = kvh * a.group + hg * kHeadsPerCta;
-    const int gc = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
+    const int vh0 = hg * kHeadsPerCta;                // first query row of this CTA within the KV head's rows
+    const int gc = min(kHeadsPerCta, a.group - vh0);
+    const int64_t sh0 = dec::item_row0<MQ>(a, s, kvh, vh0);
     const int bs = a.block_size;
     const int start = part * a.part_tokens;
     T* out = reinterpret_cast<T*>(a.out);
@@ -111,9 +112,9 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         // q[n = lane/4][k = 16*ks + 2*(lane%4) + {0,1}] and the same at k + 8.
         const int n = lane >> 2;
         const int kq = (lane & 3) * 2;
-        const int nq = min(n, gc - 1);      // lanes of absent heads read a present row, then drop it
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            reinterpret_cast<const T*>(a.q) + (static_cast<int64_t>(s) * a.num_heads + h0 + nq) * D);
+        const int nq = min(n, gc - 1);      // lanes of absent rows read a present row, then drop it
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(a.q) +
+                                                                 dec::qo_row<MQ>(a, sh0, s, kvh, vh0, nq) * D);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             ws.qb[ks][0] = n < gc ? __ldg(qrow + (ks * 16 + kq) / 2) : 0u;
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     if (L <= 0) {                                   // empty sequence: zeros
         if (part == 0)
             for (int i = threadIdx.x; i < gc * D; i += kThreads)
-                out[(static_cast<int64_t>(s) * a.num_heads + h0) * D + i] = T(0.0f);
+                out[dec::qo_row<MQ>(a, sh0, s, kvh, vh0, i / D) * D + i % D] = T(0.0f);
         return;
     }
     if (start >= L) return;                         // partition past the end of this sequence
@@ -194,6 +195,9 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
 
     // ================================================================ consumer warps
     dec::reset_state(ws);
+    // causal limits of this lane's two query-row columns (all L for decode)
+    const int lim0 = vh0 + 2 * (lane & 3) < a.group ? dec::causal_limit<MQ>(a, L, vh0 + 2 * (lane & 3)) : L;
+    const int lim1 = vh0 + 2 * (lane & 3) + 1 < a.group ? dec::causal_limit<MQ>(a, L, vh0 + 2 * (lane & 3) + 1) : L;
     bool ok = !*abort_flag;
     unsigned epi_uses = 0;
     auto epi_sync = [&]() -> bool {               // all consumer threads, bounded
@@ -213,10 +217,11 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
             ok = false;
             break;
         }
-        const int nv = min(16, end - (start + c * kChunk + warp * 16));
+        const int tokw = start + c * kChunk + warp * 16;
+        const int nv = min(16, end - tokw);
         if (nv > 0)
-            dec::consume_chunk<T, D, CW>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage), nv,
-                                         warp, lane, a.scale_log2);
+            dec::consume_chunk<T, D, CW, MQ>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage), nv,
+                                         warp, lane, a.scale_log2, tokw, lim0, lim1);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -235,8 +240,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     if (!epi_sync()) return;                      // every warp is done reading the ring
     dec::warp_state_to_smem<D, CW>(ws, scratch, warp, lane);
     if (!epi_sync()) return;
-    const int64_t sh0 = static_cast<int64_t>(s) * a.num_heads + h0;
-    dec::combine_warps<T, D, CW>(a, scratch, sh0, gc, part, nparts, threadIdx.x);
+    dec::combine_warps<T, D, CW, MQ>(a, scratch, sh0, s, kvh, vh0, gc, part, nparts, threadIdx.x);
     if (nparts == 1) return;
     // The group barrier orders every thread's partial writes before thread 0's
     // gpu-scope fence, which releases them all before the ticket.
@@ -250,14 +254,14 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     if (!epi_sync()) return;
     if (!*merge_flag) return;
     // last partition of this (sequence, head group) to finish: merge them all
-    dec::merge_partitions<T, D, CW>(a, scratch, sh0, gc, nparts, warp, lane, threadIdx.x, epi_sync);
+    dec::merge_partitions<T, D, CW, MQ>(a, scratch, sh0, s, kvh, vh0, gc, nparts, warp, lane, threadIdx.x, epi_sync);
 }
 
-template <typename T, int D, int CW, int STAGES>
+template <typename T, int D, int CW, int STAGES, bool MQ = false>
 cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
     constexpr size_t smem = Smem<D, CW, STAGES>::kBytes;
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = decode_kernel<T, D, CW, STAGES>;
+    auto kern = decode_kernel<T, D, CW, STAGES, MQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(static_cast<unsigned>(a.num_kv_heads * a.head_groups), static_cast<unsigned>(a.max_parts),
@@ -269,6 +273,7 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensor
 template <typename T, int D>
 cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int warps, int stages,
                        cudaStream_t s) {
+    if (a.num_queries > 1) return launch_t<T, D, 4, 2, true>(a, tmk, tmv, s);   // verify: one shape
     if (warps == 2) {
         switch (stages) {
             case 2: return launch_t<T, D, 2, 2>(a, tmk, tmv, s);
@@ -320,7 +325,7 @@ namespace {
 template <typename T, int D, int CW, int STAGES>
 int occupancy_of() {
     constexpr size_t smem = Smem<D, CW, STAGES>::kBytes;
-    auto kern = decode_kernel<T, D, CW, STAGES>;
+    auto kern = decode_kernel<T, D, CW, STAGES, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return 0;
     int n = 0;
@@ -369,8 +374,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
         const char* e = getenv("PKV_DECODE_VARIANT");
         return e && e[0] == 'p';
     }();
-    return persistent ? launch_decode_persistent(a, tmk, tmv, dtype, head_dim, s)
-                      : launch_decode_grid(a, tmk, tmv, dtype, head_dim, s);
+    // the persistent kernel serves one query token per sequence
+    return persistent && a.num_queries == 1 ? launch_decode_persistent(a, tmk, tmv, dtype, head_dim, s)
+                                            : launch_decode_grid(a, tmk, tmv, dtype, head_dim, s);
 }
 
 }  // namespace pkv

@@ -51,6 +51,45 @@ __device__ __forceinline__ void raise_abort(unsigned* err, volatile int* abort_f
     *abort_flag = 1;
 }
 
+// MQ (template flag) selects the multi-query (verify) form of the helpers
+// below; the decode kernels compile with MQ = false and carry none of it.
+//
+// Query rows.  A KV head serves `group` query rows: for query token i of the
+// sequence (0 <= i < num_queries) and query head hl of the KV head's
+// `qgroup`, row vh = i * qgroup + hl.  q and out are [B][num_queries][Hq][D].
+// An item (sequence s, KV head kvh, rows vh0 .. vh0 + 7) is addressed by
+// sh0, the row of vh0 in the split-K partials ([B][Hq * nq][parts]); with one
+// query token that is also the row of vh0 in q and out, and row vh0 + hx is
+// sh0 + hx in all three.
+template <bool MQ>
+__device__ __forceinline__ int64_t item_row0(const DecodeArgs& a, int s, int kvh, int vh0) {
+    if constexpr (MQ)
+        return static_cast<int64_t>(s) * a.num_heads * a.num_queries + static_cast<int64_t>(kvh) * a.group + vh0;
+    else
+        return static_cast<int64_t>(s) * a.num_heads + kvh * a.group + vh0;
+}
+
+// Row of q / out (element offset / D) of the item's row vh0 + hx.
+template <bool MQ>
+__device__ __forceinline__ int64_t qo_row(const DecodeArgs& a, int64_t sh0, int s, int kvh, int vh0, int hx) {
+    if constexpr (MQ) {
+        const int vh = vh0 + hx;
+        const int i = vh / a.qgroup;
+        const int hl = vh - i * a.qgroup;
+        return (static_cast<int64_t>(s) * a.num_queries + i) * a.num_heads + kvh * a.qgroup + hl;
+    } else {
+        return sh0 + hx;
+    }
+}
+
+// Exclusive causal limit of query row vh: query token i of a sequence of L
+// positions (its last num_queries being the queries' own) sees positions
+// < L - num_queries + i + 1; for decode (one query) that is all L positions.
+template <bool MQ>
+__device__ __forceinline__ int causal_limit(const DecodeArgs& a, int L, int vh) {
+    return MQ ? L - a.num_queries + vh / a.qgroup + 1 : L;
+}
+
 // One consumer warp's running state for one work item: O^T accumulators
 // (d x 8 heads, fp32), running max and sum of its two head columns, and the
 // Q^T operand fragments.
@@ -72,10 +111,11 @@ __device__ __forceinline__ void reset_state(WarpState<D>& w) {
 // One warp's 16 positions of a chunk: S^T = K Q^T on the tensor cores, online
 // softmax over those scores (log2 domain, positions >= nv masked), then
 // O^T += V^T P^T.  `warp` selects the 16 rows of the chunk; kst / vst are the
-// stage's K and V ring addresses.
-template <typename T, int D, int CW>
+// stage's K and V ring addresses; tokw is the position of the warp's first
+// row and lim0 / lim1 the causal limits of this lane's two head columns.
+template <typename T, int D, int CW, bool MQ>
 __device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uint32_t vst, int nv, int warp, int lane,
-                                              float sl2) {
+                                              float sl2, int tokw, int lim0, int lim1) {
     using G = Geo<D, CW>;
     using M = Mma<T>;
     const int krow = warp * 16 + (lane & 15);                     // ldmatrix row supplied by this lane (K)
@@ -105,10 +145,12 @@ __device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uin
     }
     // ---- online softmax (log2 domain); columns are heads 2*(lane%4) + {0,1}
     const bool va = r0 < nv, vb = r0 + 8 < nv;
-    const float s0 = va ? sacc[0] * sl2 : -INFINITY;
-    const float s1 = va ? sacc[1] * sl2 : -INFINITY;
-    const float s2 = vb ? sacc[2] * sl2 : -INFINITY;
-    const float s3 = vb ? sacc[3] * sl2 : -INFINITY;
+    const int pa = tokw + r0, pb = pa + 8;
+    // decode: every column sees every row below nv; verify: also below the column's causal limit
+    const float s0 = (va && (!MQ || pa < lim0)) ? sacc[0] * sl2 : -INFINITY;
+    const float s1 = (va && (!MQ || pa < lim1)) ? sacc[1] * sl2 : -INFINITY;
+    const float s2 = (vb && (!MQ || pb < lim0)) ? sacc[2] * sl2 : -INFINITY;
+    const float s3 = (vb && (!MQ || pb < lim1)) ? sacc[3] * sl2 : -INFINITY;
     float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -116,11 +158,15 @@ __device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uin
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(w.m0, mx0), mn1 = fmaxf(w.m1, mx1);
-    const float al0 = fast_exp2(w.m0 - mn0), al1 = fast_exp2(w.m1 - mn1);
+    // verify: a column with no visible position yet keeps max -inf: scale 1, weights 0
+    // (decode never has one: row 0 of the warp is always visible)
+    const float al0 = (MQ && mn0 == -INFINITY) ? 1.0f : fast_exp2(w.m0 - mn0);
+    const float al1 = (MQ && mn1 == -INFINITY) ? 1.0f : fast_exp2(w.m1 - mn1);
     w.m0 = mn0;
     w.m1 = mn1;
-    const uint32_t p01 = M::pack(fast_exp2(s0 - mn0), fast_exp2(s1 - mn1));
-    const uint32_t p23 = M::pack(fast_exp2(s2 - mn0), fast_exp2(s3 - mn1));
+    const float b0 = (MQ && mn0 == -INFINITY) ? 0.0f : mn0, b1 = (MQ && mn1 == -INFINITY) ? 0.0f : mn1;
+    const uint32_t p01 = M::pack(fast_exp2(s0 - b0), fast_exp2(s1 - b1));
+    const uint32_t p23 = M::pack(fast_exp2(s2 - b0), fast_exp2(s3 - b1));
     const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);   // the weights PV actually uses
     w.l0 = w.l0 * al0 + f01.x + f23.x;
     w.l1 = w.l1 * al1 + f01.y + f23.y;
@@ -177,9 +223,9 @@ __device__ __forceinline__ void warp_state_to_smem(const WarpState<D>& w, float*
 // Combine the warps' states of one item (scratch written and synchronised):
 // a sequence of one partition gets its output; otherwise the partition's
 // (max, sum, unnormalised output) go to the workspace.
-template <typename T, int D, int CW>
-__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* scratch, int64_t sh0, int gc, int part,
-                                              int nparts, int tid) {
+template <typename T, int D, int CW, bool MQ>
+__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* scratch, int64_t sh0, int s, int kvh,
+                                              int vh0, int gc, int part, int nparts, int tid) {
     const float* sm_m = scratch;
     const float* sm_l = sm_m + CW * kHeadsPerCta;
     const float* sm_o = sm_l + CW * kHeadsPerCta;
@@ -193,14 +239,16 @@ __device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* 
         float den = 0.0f, num = 0.0f;
 #pragma unroll
         for (int w = 0; w < CW; ++w) {
-            const float wt = fast_exp2(sm_m[w * kHeadsPerCta + hx] - mx);
+            const float mw = sm_m[w * kHeadsPerCta + hx];
+            // verify: a warp that saw nothing adds nothing (decode: mx is finite, the weight is 0 anyway)
+            const float wt = (MQ && mw == -INFINITY) ? 0.0f : fast_exp2(mw - mx);
             den += wt * sm_l[w * kHeadsPerCta + hx];
             num += wt * sm_o[(w * kHeadsPerCta + hx) * D + d];
         }
-        const int64_t sh = sh0 + hx;
         if (nparts == 1) {
-            out[sh * D + d] = T(num / den);
+            out[qo_row<MQ>(a, sh0, s, kvh, vh0, hx) * D + d] = T(MQ ? (den > 0.0f ? num / den : 0.0f) : num / den);
         } else {
+            const int64_t sh = sh0 + hx;
             a.ws_o[(sh * a.max_parts + part) * D + d] = num;
             if (d == 0) a.ws_ml[sh * a.max_parts + part] = make_float2(mx, den);
         }
@@ -211,9 +259,9 @@ __device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* 
 // CTA that took the last ticket.  Phase A (one warp per head): the maximum and
 // the denominator, into msm[8] / dsm[8].  `sync` separates the phases.
 // Phase B: each output element sums its partials with all their loads in flight.
-template <typename T, int D, int CW, typename Sync>
-__device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scratch, int64_t sh0, int gc, int nparts,
-                                                 int warp, int lane, int tid, Sync&& sync) {
+template <typename T, int D, int CW, bool MQ, typename Sync>
+__device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scratch, int64_t sh0, int s, int kvh,
+                                                 int vh0, int gc, int nparts, int warp, int lane, int tid, Sync&& sync) {
     float* msm = scratch;
     float* dsm = scratch + kHeadsPerCta;
     for (int hx = warp; hx < gc; hx += CW) {
@@ -283,7 +331,9 @@ __device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scr
 #pragma unroll
         for (int k = 0; k < kAcc; ++k) {
             const int hx = hb + k * kRows;
-            if (hx < gc) out[(sh0 + hx) * D + d] = T(num[k] / dsm[hx]);
+            if (hx < gc)
+                out[qo_row<MQ>(a, sh0, s, kvh, vh0, hx) * D + d] =
+                    T(MQ ? (dsm[hx] > 0.0f ? num[k] / dsm[hx] : 0.0f) : num[k] / dsm[hx]);
         }
     }
     return true;

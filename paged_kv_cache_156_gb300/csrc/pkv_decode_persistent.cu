@@ -93,7 +93,8 @@ struct ChunkInfo {
     int nvalid;   // positions of the chunk below seq_len
     int flags;    // kFirst / kLast chunk of its unit
     int nparts;   // partitions of the sequence
-    int pad0, pad1;
+    int tok0w;    // position of the chunk's first row
+    int L;        // sequence length
 };
 
 template <int D, int CW, int STAGES>
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent
             const int nch = (end - start + kChunk - 1) / kChunk;
             const int hg = hh % a.head_groups;
             const int kvh = hh / a.head_groups;
-            const int h0 = kvh * a.group + hg * kHeadsPerCta;
+            const int h0 = kvh * a.qgroup + hg * kHeadsPerCta;   // one query token: rows are heads
             const int gc = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
             const int per_chunk = kChunk / bs;
             const int* tb = tbl + slot * kMaxTable;
@@ -258,6 +259,8 @@ __global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent
                 in.nvalid = nv;
                 in.flags = (ci == 0 ? kFirst : 0) | (ci == nch - 1 ? kLast : 0);
                 in.nparts = nparts;
+                in.tok0w = tok0;
+                in.L = L;
                 const unsigned qbytes = ci == 0 ? static_cast<unsigned>(gc * D * 2) : 0u;
                 mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * 2 * 2) + qbytes);
                 if (ci == 0)
@@ -313,8 +316,10 @@ __global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent
         if (ci.s < 0) break;
         ++c;
         const int hg = ci.hh % a.head_groups;
-        const int h0 = (ci.hh / a.head_groups) * a.group + hg * kHeadsPerCta;
-        const int gc = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
+        const int kvh = ci.hh / a.head_groups;
+        const int vh0 = hg * kHeadsPerCta;
+        const int gc = min(kHeadsPerCta, a.group - vh0);
+        const int64_t sh0 = dec::item_row0<false>(a, ci.s, kvh, vh0);
         if (ci.flags & kFirst) {
             // Q^T fragments from the unit's query rows (rows of absent heads are zero)
             const uint32_t* qs = reinterpret_cast<const uint32_t*>(qslots + st * S::kQSlot);
@@ -330,8 +335,8 @@ __global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent
         const int nv = min(16, ci.nvalid - warp * 16);
         uint8_t* stage = smem + st * S::kStagePair;
         if (nv > 0)
-            dec::consume_chunk<T, D, CW>(ws, smem_u32(stage), smem_u32(stage + G::kStage), nv, warp, lane,
-                                         a.scale_log2);
+            dec::consume_chunk<T, D, CW, false>(ws, smem_u32(stage), smem_u32(stage + G::kStage), nv, warp, lane,
+                                         a.scale_log2, ci.tok0w + warp * 16, ci.L, ci.L);
         __syncwarp();
         if (!(ci.flags & kLast)) {
             if (lane == 0) mbar_arrive(&empty[st]);
@@ -343,8 +348,7 @@ __global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent
         if (!epi_sync()) break;                   // every warp is done reading this stage
         dec::warp_state_to_smem<D, CW>(ws, scratch, warp, lane);
         if (!epi_sync()) break;
-        const int64_t sh0 = static_cast<int64_t>(ci.s) * a.num_heads + h0;
-        dec::combine_warps<T, D, CW>(a, scratch, sh0, gc, ci.part, ci.nparts, threadIdx.x);
+        dec::combine_warps<T, D, CW, false>(a, scratch, sh0, ci.s, kvh, vh0, gc, ci.part, ci.nparts, threadIdx.x);
         if (ci.nparts > 1) {
             // the group barrier orders every thread's partial writes before thread
             // 0's gpu-scope fence, which releases them all before the ticket
@@ -357,8 +361,8 @@ __global__ void __launch_bounds__(persistent_threads<D, CW>()) decode_persistent
             }
             if (!epi_sync()) break;
             if (*merge_flag) {
-                if (!dec::merge_partitions<T, D, CW>(a, scratch, sh0, gc, ci.nparts, warp, lane, threadIdx.x,
-                                                     epi_sync))
+                if (!dec::merge_partitions<T, D, CW, false>(a, scratch, sh0, ci.s, kvh, vh0, gc, ci.nparts, warp, lane,
+                                                           threadIdx.x, epi_sync))
                     break;
             }
         }

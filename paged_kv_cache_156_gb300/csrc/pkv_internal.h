@@ -56,8 +56,10 @@ struct DecodeArgs {
     int num_seqs;
     int num_heads;
     int num_kv_heads;
-    int group;                       // num_heads / num_kv_heads
-    int head_groups;                 // ceil(group / 8): query-head groups per KV head
+    int group;                       // query rows per KV head: (num_heads / num_kv_heads) * num_queries
+    int qgroup;                      // query heads per KV head: num_heads / num_kv_heads
+    int num_queries;                 // query tokens per sequence (1 = decode; > 1 = verify, causal)
+    int head_groups;                 // ceil(group / 8): groups of query rows per KV head
     int block_size;
     int part_tokens;                 // tokens per partition (multiple of 64)
     int max_parts;                   // ceil(max_seq_len / part_tokens)

@@ -1,0 +1,71 @@
+"""GPU parity of paged_attention_verify (multi-query, causal) against the oracle.
+
+The last num_queries positions of each sequence are the query tokens' own K/V;
+query token i sees positions < L - num_queries + i + 1.  Cases cover query
+rows that fit one 8-row group and several, one and several partitions, query
+tokens that see nothing in a late partition, and every block size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_156_gb300 as pkv
+import workloads as W
+from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_caches_after_step, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_error_word():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pkv.device_error(reset=True)
+    yield
+    assert pkv.device_error(reset=True) == 0
+
+
+CASES = [
+    dict(num_heads=16, num_kv_heads=4, head_dim=128, block_size=16, dtype=W.BF16, nq=2,
+         lens=("fixed", (2, 40, 1025, 300))),
+    dict(num_heads=64, num_kv_heads=8, head_dim=128, block_size=8, dtype=W.F16, nq=4,
+         lens=("fixed", (4, 1025, 700, 64, 65))),
+    dict(num_heads=4, num_kv_heads=4, head_dim=64, block_size=32, dtype=W.F16, nq=3, lens=("fixed", (3, 17, 2000))),
+    dict(num_heads=12, num_kv_heads=4, head_dim=128, block_size=16, dtype=W.BF16, nq=5, lens=("fixed", (130, 5, 513))),
+]
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 64, 1024])
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_verify_matches_oracle(case, partition_tokens):
+    kw = dict(CASES[case])
+    nq = kw.pop("nq")
+    kw["num_seqs"] = len(kw["lens"][1])
+    wl = W.build(W.small_spec(seed=300 + case, **kw))
+    step = DeviceStep(wl)
+    pkv.paged_kv_append(step.k_new, step.v_new, step.kc[0], step.vc[0], step.slot_mapping)
+    rng = np.random.default_rng(case)
+    s = wl.spec
+    q = W.normal_bits(rng, (s.num_seqs, nq, s.num_heads, s.head_dim), s.dtype)
+    qd = to_dev(q, s.dtype)
+    out = torch.full_like(qd, float("nan"))
+    pkv.paged_attention_verify(out, qd, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
+                               max_seq_len=wl.max_seq_len, partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
+    ref = oracle.verify_attention_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
+    assert torch.isfinite(out).all()
+    err = max_abs_err(out, ref)
+    assert err <= TOL[s.dtype], f"max abs err {err}"
+
+
+def test_one_query_verify_is_the_decode_call():
+    wl = W.build(W.small_spec(num_seqs=4, num_heads=32, num_kv_heads=8, dtype=W.BF16,
+                              lens=("fixed", (900, 33, 2049, 1))))
+    step = DeviceStep(wl, partition_tokens=256)
+    step.run()
+    out = torch.empty_like(step.q).unsqueeze(1)
+    pkv.paged_attention_verify(out, step.q.unsqueeze(1).contiguous(), step.kc[0], step.vc[0], step.block_tables,
+                               step.seq_lens, wl.scale, max_seq_len=wl.max_seq_len, partition_tokens=256)
+    torch.cuda.synchronize()
+    assert torch.equal(out[:, 0], step.out[0])

@@ -458,10 +458,54 @@ def check_cow_shared_equals_private():
         assert np.array_equal(shared[f], priv[0])
 
 
+def check_verify_reduces_to_decode_and_truncation():
+    """One query token is the decode call; query token i of nq equals the decode of the
+    sequence cut at its causal limit L - nq + i + 1."""
+    rng = np.random.default_rng(11)
+    Hq, Hkv, d, bs, nq = 8, 2, 16, 8, 3
+    lens = np.array([9, 30, 3])
+    NB = 20
+    perm = rng.permutation(NB)
+    tables = np.full((3, 4), 77, np.int64)
+    k = 0
+    for s_ in range(3):
+        for j in range(-(-lens[s_] // bs)):
+            tables[s_, j] = perm[k]
+            k += 1
+    kc = bits(rng.standard_normal((NB, bs, Hkv, d)))
+    vc = bits(rng.standard_normal((NB, bs, Hkv, d)))
+    q = bits(rng.standard_normal((3, nq, Hq, d)))
+    one = oracle.verify_attention_ref(q[:, :1], kc, vc, tables, lens, 0.3, Hkv, F16)
+    assert np.array_equal(one[:, 0], oracle.attention_ref(q[:, 0], kc, vc, tables, lens, 0.3, Hkv, F16))
+    got = oracle.verify_attention_ref(q, kc, vc, tables, lens, 0.3, Hkv, F16)
+    for i in range(nq):
+        cut = lens - nq + i + 1
+        want = oracle.attention_ref(q[:, i], kc, vc, tables, cut, 0.3, Hkv, F16)
+        assert np.array_equal(got[:, i], want)
+
+
+def check_verify_is_causal():
+    """Keys after a query's limit cannot move its output, however large their scores."""
+    rng = np.random.default_rng(12)
+    d, bs, nq, L = 8, 16, 4, 12
+    K = rng.standard_normal((L, 1, d)) * 0.1
+    V = rng.standard_normal((L, 1, d))
+    q = bits(np.ones((1, nq, 1, d)))
+    kc, vc, table = contiguous_pool(K, V, bs)
+    base = oracle.verify_attention_ref(q, kc, vc, table[None], np.array([L]), 1.0, 1, F16)
+    K2 = K.copy()
+    K2[L - 1] = 50.0                          # only query nq-1 may see position L-1
+    kc2, vc2, _ = contiguous_pool(K2, V, bs)
+    moved = oracle.verify_attention_ref(q, kc2, vc2, table[None], np.array([L]), 1.0, 1, F16)
+    assert np.array_equal(base[0, :nq - 1], moved[0, :nq - 1])
+    assert np.allclose(moved[0, nq - 1, 0], oracle.decode_bits(bits(V[L - 1, 0]), F16), atol=1e-10)
+
+
 PINS = [check_closed_form_two_tokens, check_single_token_returns_v, check_identical_keys_give_mean_of_v,
         check_dominant_key, check_large_scores_stay_finite, check_gqa_mapping, check_gqa_equals_replicated_mha,
         check_permutation_and_block_size_invariance, check_brute_force_tiny, check_tail_never_read,
-        check_merge_identity, check_empty_sequence_is_zero, check_cow_shared_equals_private]
+        check_merge_identity, check_empty_sequence_is_zero, check_cow_shared_equals_private,
+        check_verify_reduces_to_decode_and_truncation, check_verify_is_causal]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
