@@ -264,12 +264,17 @@ def run_pkv(args, rank, world, local):
             vcs.append(v)
         pools.append((kcs, vcs))
     outs = [torch.empty_like(q) for _ in range(spec.num_layers)]
-    part = args.partition_tokens or pkv.decode_partition_tokens(spec.num_seqs, spec.num_heads, spec.num_kv_heads,
-                                                                spec.head_dim, wl.max_seq_len)
-    ws = pkv.alloc_workspace(spec.num_seqs, spec.num_heads, spec.num_kv_heads, spec.head_dim, wl.max_seq_len, part,
-                             dev)
-    max_parts = math.ceil(wl.max_seq_len / part) if wl.max_seq_len else 1
-    launches_per_step = (1 if len(wl.copy_pairs) else 0) + spec.num_layers * (2 + (1 if max_parts > 1 else 0))
+    # 0 = automatic: the host sizes the workspace for the smallest partition,
+    # the plan kernel picks the size from the lengths
+    part_min = args.partition_tokens or pkv.decode_partition_tokens(spec.num_seqs, spec.num_heads,
+                                                                    spec.num_kv_heads, spec.head_dim, wl.max_seq_len)
+    ws = pkv.alloc_workspace(spec.num_seqs, spec.num_heads, spec.num_kv_heads, spec.head_dim, wl.max_seq_len,
+                             args.partition_tokens, dev)
+    planned = spec.num_seqs <= pkv.PLAN_MAX_SEQS
+    max_parts_min = math.ceil(wl.max_seq_len / part_min) if wl.max_seq_len else 1
+    # per layer: append, plan kernel (or the ticket memset of an unplanned split batch), decode
+    launches_per_step = (1 if len(wl.copy_pairs) else 0) + spec.num_layers * (
+        2 + (1 if planned or max_parts_min > 1 else 0))
 
     ev_pairs = []
 
@@ -284,7 +289,8 @@ def run_pkv(args, rank, world, local):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
             pkv.paged_attention_decode(outs[l], q, kcs[l], vcs[l], tables, lens, wl.scale,
-                                       max_seq_len=wl.max_seq_len, workspace=ws, partition_tokens=part)
+                                       max_seq_len=wl.max_seq_len, workspace=ws,
+                                       partition_tokens=args.partition_tokens)
             if rec:
                 b.record()
                 ev_pairs.append((a, b))
@@ -293,6 +299,9 @@ def run_pkv(args, rank, world, local):
         step(i, False)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0, "device error word raised during warm-up"
+    part = pkv.decode_plan_partition_tokens(ws, spec.num_seqs, spec.num_heads, spec.num_kv_heads) if planned \
+        else part_min
+    max_parts = math.ceil(wl.max_seq_len / part) if wl.max_seq_len else 1
 
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     time.sleep(0.3)
@@ -373,13 +382,14 @@ def run_pkv(args, rank, world, local):
                    "block_size": spec.block_size, "num_layers": spec.num_layers,
                    "mean_seq_len": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
                    "num_blocks": wl.num_blocks, "copy_pairs": int(len(wl.copy_pairs)),
-                   "partition_tokens": part, "max_partitions": max_parts,
+                   "partition_tokens": part, "partition_tokens_min": part_min, "max_partitions": max_parts,
+                   "work_list": "plan kernel" if planned else "full grid",
                    "l2": f"inputs larger than L2: {replicas} rotating pool replicas of "
                          f"{footprint / 1e9:.3f} GB each (L2 {L2_BYTES / 2**20:.0f} MiB)",
                    "parallelism": f"replicas x{world} (no data-path collective)"},
         "tokens_per_s": round(world * spec.num_seqs * args.steps / (max_ms / 1e3), 1),
         "step_bytes": nbytes,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel (paged_attention_decode call: ticket memset + partition kernel with in-kernel split-K merge; layer 0)",
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (paged_attention_decode call: plan kernel + partition kernel with in-kernel split-K merge; layer 0)",
                      "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": nbytes["decode_unique"], "avg_launch_ms": round(dec_ms, 5)},

@@ -91,18 +91,36 @@ PKV_API pkv_status pkv_paged_kv_append(const void* k, const void* v, void* key_c
                                void* stream);
 
 /*
- * Workspace for pkv_paged_attention_decode: bytes needed for its work counter,
- * per-(sequence, head group) merge tickets and the split-K partials (never 0).
- * partition_tokens: 0 picks the size the decode call picks for the same
- * arguments on the current device; otherwise the caller's partition size.
- * Returns (size_t)-1 for invalid arguments.
+ * Workspace for pkv_paged_attention_decode: bytes needed for its
+ * per-(sequence, head group) merge tickets, its work list and the split-K
+ * partials (never 0).  partition_tokens: 0 sizes it for the smallest
+ * partition the decode call may use for the same arguments on the current
+ * device; otherwise for the caller's partition size.  Returns (size_t)-1 for
+ * invalid arguments.
  */
 PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                   int max_seq_len, int partition_tokens);
 
-/* Partition size (tokens) pkv_paged_attention_decode uses when passed 0, or -1 on bad arguments. */
+/*
+ * Smallest partition size (tokens) pkv_paged_attention_decode uses when
+ * passed 0 (its device-side plan may take a larger one from the actual
+ * lengths, see below), or -1 on bad arguments.
+ */
 PKV_API int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                 int max_seq_len);
+
+/* Batches of up to this many sequences run through the plan kernel (below). */
+#define PKV_PLAN_MAX_SEQS 1024
+
+/*
+ * Partition size (tokens) the last pkv_paged_attention_decode call with this
+ * workspace and batch shape used, read back from its work list (synchronises
+ * `stream`); -1 for a batch above PKV_PLAN_MAX_SEQS (no work list), bad
+ * arguments or a failed read.  For pkv_paged_attention_verify pass
+ * num_heads * num_queries.
+ */
+PKV_API int pkv_decode_plan_partition_tokens(const void* workspace, int num_seqs, int num_heads, int num_kv_heads,
+                                     void* stream);
 
 /*
  * paged_attention_decode -- one query token per sequence attends over its
@@ -124,7 +142,9 @@ PKV_API int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_
  *   value_cache   [num_blocks][block_size][num_kv_heads][head_dim]
  *   block_tables  int32 [num_seqs][max_blocks_per_seq]; only the first
  *                 ceil(seq_lens[s] / block_size) entries of row s are read
- *   seq_lens      int32 [num_seqs], each in [0, max_seq_len]
+ *   seq_lens      int32 [num_seqs], each in [0, max_seq_len] (a length above
+ *                 it is treated as max_seq_len and raises the device error
+ *                 word)
  *   max_seq_len   host-known upper bound of seq_lens (sizes the launch; it
  *                 must not exceed max_blocks_per_seq * block_size)
  *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
@@ -135,7 +155,13 @@ PKV_API int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_
  *                 Sequences longer than one partition are split into
  *                 partitions whose partial softmax states are merged in the
  *                 same launch by the last partition to finish (split-K over
- *                 the sequence).
+ *                 the sequence).  For up to 1024 sequences a plan kernel
+ *                 first lists the (sequence, partition) items that exist,
+ *                 longest sequences first, and with 0 picks the partition
+ *                 size from the lengths themselves (about 0.85 x the
+ *                 positions per resident CTA, multiples of 512, at least
+ *                 pkv_decode_partition_tokens); the output does not depend
+ *                 on that order.
  * head_dim in {64, 128}; block_size in {8, 16, 32}; num_heads a multiple of
  * num_kv_heads.
  */

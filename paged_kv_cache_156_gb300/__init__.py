@@ -22,10 +22,11 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
 
 PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_OOM = range(6)
 _DT = {torch.float16: 0, torch.bfloat16: 1}
+PLAN_MAX_SEQS = 1024        # PKV_PLAN_MAX_SEQS: batches up to this size run through the plan kernel
 
 # every symbol include/pkv.h declares
 ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
-               "pkv_decode_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
+               "pkv_decode_partition_tokens", "pkv_decode_plan_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
                "pkv_paged_attention_decode_static", "pkv_swap_blocks", "pkv_paged_attention_verify", "pkv_bm_create", "pkv_bm_destroy",
                "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
                "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables")
@@ -58,6 +59,8 @@ def load() -> ctypes.CDLL:
     lib.pkv_decode_workspace_bytes.argtypes = [c_i, c_i, c_i, c_i, c_i, c_i]
     lib.pkv_decode_partition_tokens.restype = c_i
     lib.pkv_decode_partition_tokens.argtypes = [c_i, c_i, c_i, c_i, c_i]
+    lib.pkv_decode_plan_partition_tokens.restype = c_i
+    lib.pkv_decode_plan_partition_tokens.argtypes = [c_p, c_i, c_i, c_i, c_p]
     lib.pkv_paged_attention_decode.restype = c_i
     lib.pkv_paged_attention_decode.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
@@ -135,6 +138,12 @@ def paged_kv_append(k, v, key_cache, value_cache, slot_mapping) -> None:
 
 def decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) -> int:
     return int(load().pkv_decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len))
+
+
+def decode_plan_partition_tokens(workspace, num_seqs, num_heads, num_kv_heads) -> int:
+    """Partition size the last decode call with ``workspace`` used (-1: unplanned batch); synchronises."""
+    return int(load().pkv_decode_plan_partition_tokens(_cuda("workspace", workspace), num_seqs, num_heads,
+                                                       num_kv_heads, _stream(workspace)))
 
 
 def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, partition_tokens=0) -> int:

@@ -16,6 +16,8 @@
 // Device error word (bit meanings in include/pkv.h, pkv_device_error).
 __device__ unsigned int g_pkv_error_word;
 
+static_assert(PKV_PLAN_MAX_SEQS == pkv::kPlanMaxSeqs, "plan batch limit: header and kernels agree");
+
 namespace {
 
 thread_local char g_msg[512] = "";
@@ -219,6 +221,21 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
     return workspace_for(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, part);
 }
 
+int pkv_decode_plan_partition_tokens(const void* workspace, int num_seqs, int num_heads, int num_kv_heads,
+                                     void* stream) {
+    if (!workspace || num_seqs <= 0 || num_seqs > pkv::kPlanMaxSeqs || num_kv_heads <= 0 || num_heads <= 0 ||
+        num_heads % num_kv_heads != 0)
+        return -1;
+    const pkv::DecodeWorkspace lay = pkv::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, 64, 1);
+    int4 first;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&first, static_cast<const char*>(workspace) + lay.ticket_bytes, sizeof(first),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return -1;
+    return first.w;
+}
+
 int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len) {
     if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len) != PKV_OK) return -1;
     return resolve_partition(num_seqs, num_heads, num_kv_heads, max_seq_len, 0, head_dim);
@@ -282,12 +299,10 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.block_tables = block_tables;
     a.seq_lens = seq_lens;
     char* ws = static_cast<char*>(workspace);
-    a.work_counter = reinterpret_cast<unsigned*>(ws);
-    a.n_items = a.work_counter + 1;
-    a.tickets = a.work_counter + 2;
-    a.items = reinterpret_cast<unsigned*>(ws + lay.ticket_bytes);
-    a.ws_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ticket_bytes + lay.item_bytes) : nullptr;
-    a.ws_ml = max_parts > 1 ? reinterpret_cast<float2*>(ws + lay.ticket_bytes + lay.item_bytes + lay.o_bytes)
+    a.tickets = reinterpret_cast<unsigned*>(ws);
+    a.plan = num_seqs <= pkv::kPlanMaxSeqs ? reinterpret_cast<int4*>(ws + lay.ticket_bytes) : nullptr;
+    a.ws_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ticket_bytes + lay.plan_bytes) : nullptr;
+    a.ws_ml = max_parts > 1 ? reinterpret_cast<float2*>(ws + lay.ticket_bytes + lay.plan_bytes + lay.o_bytes)
                             : nullptr;
     a.err = error_word(dev);
     a.num_blocks = num_blocks;
@@ -301,7 +316,11 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.head_groups = (a.group + 7) / 8;
     a.block_size = block_size;
     a.part_tokens = part;
+    a.part_auto = partition_tokens == 0;
+    a.slots = sm_count_of(dev) * pkv::decode_ctas_per_sm(head_dim);
+    a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
+    a.plan_capacity = num_seqs * static_cast<int>(max_parts);
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));

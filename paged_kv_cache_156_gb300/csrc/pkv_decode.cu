@@ -7,11 +7,14 @@
 //
 // How (sm_103a):
 //  * One CTA per work item = (KV head, group of <= 8 query heads sharing it,
-//    partition of part_tokens positions, sequence).  All query heads of a KV
-//    head are served from the same K/V bytes, so every byte of the pool is
-//    read from HBM once per step.  Two or three CTAs share an SM so one CTA's
-//    start-up (table and q fetch, first loads in flight) hides behind the
-//    others' streaming.
+//    partition of P positions, sequence).  All query heads of a KV head are
+//    served from the same K/V bytes, so every byte of the pool is read from
+//    HBM once per step.  Two or three CTAs share an SM so one CTA's start-up
+//    (table and q fetch, first loads in flight) hides behind the others'
+//    streaming.  The items come from the plan kernel's work list (only the
+//    partitions that exist, long sequences first, P chosen from the batch's
+//    lengths); a batch too large to plan runs the full grid instead, whose
+//    CTAs past their sequence's end return at once.
 //  * The CTA's slice of the block table is staged in shared memory once; a
 //    producer warp then streams the partition's K and V tiles with TMA
 //    (cp.async.bulk.tensor; one box = one (physical block, KV head) tile of
@@ -80,16 +83,33 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int hh = blockIdx.x;                    // KV head * head_groups + query-head group
-    const int part = blockIdx.y;
-    const int s = blockIdx.z;
+    // Work item: from the plan (one entry per (sequence, partition), KV head
+    // groups innermost in the 1-D grid) or, without one, the 3-D grid itself.
+    int hh, part, s, P, Lp;
+    if (a.plan) {
+        const int nh = a.num_kv_heads * a.head_groups;
+        const unsigned y = blockIdx.x / static_cast<unsigned>(nh);
+        hh = static_cast<int>(blockIdx.x - y * static_cast<unsigned>(nh));
+        const int4 it = __ldg(a.plan + y);
+        s = it.x;
+        part = it.y;
+        Lp = it.z;
+        P = it.w;
+        if (s < 0) return;                          // padding entry
+    } else {
+        hh = blockIdx.x;                            // KV head * head_groups + query-head group
+        part = blockIdx.y;
+        s = blockIdx.z;
+        P = a.part_tokens;
+        Lp = -1;
+    }
     const int hg = hh % a.head_groups;
     const int kvh = hh / a.head_groups;
     const int vh0 = hg * kHeadsPerCta;                // first query row of this CTA within the KV head's rows
     const int gc = min(kHeadsPerCta, a.group - vh0);
     const int64_t sh0 = dec::item_row0<MQ>(a, s, kvh, vh0);
     const int bs = a.block_size;
-    const int start = part * a.part_tokens;
+    const int start = part * P;
     T* out = reinterpret_cast<T*>(a.out);
 
     // Issue the loads that depend only on the work item before the sequence
@@ -99,7 +119,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     int te[kTePerLane];
     dec::WarpState<D> ws;
     const int first_blk = start / bs;
-    const int tcount = min(a.part_tokens / bs, a.max_blocks_per_seq - first_blk);
+    const int tcount = min(P / bs, a.max_blocks_per_seq - first_blk);
     if (warp == CW) {
         const int32_t* row = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + first_blk;
 #pragma unroll
@@ -122,7 +142,14 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         }
     }
 
-    const int L = __ldg(a.seq_lens + s);
+    int L = Lp;
+    if (Lp < 0) {
+        L = __ldg(a.seq_lens + s);
+        if (L > a.max_seq_len) {                    // precondition broken: attend over max_seq_len
+            if (threadIdx.x == 0 && part == 0 && hh == 0) raise_error(a.err, kErrBounds);
+            L = a.max_seq_len;
+        }
+    }
     if (L <= 0) {                                   // empty sequence: zeros
         if (part == 0)
             for (int i = threadIdx.x; i < gc * D; i += kThreads)
@@ -130,8 +157,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         return;
     }
     if (start >= L) return;                         // partition past the end of this sequence
-    const int end = min(L, start + a.part_tokens);
-    const int nparts = (L + a.part_tokens - 1) / a.part_tokens;
+    const int end = min(L, start + P);
+    const int nparts = (L + P - 1) / P;
     const int nchunks = (end - start + kChunk - 1) / kChunk;
 
     if (threadIdx.x == 0) {
@@ -264,8 +291,9 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensor
     auto kern = decode_kernel<T, D, CW, STAGES, MQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(a.num_kv_heads * a.head_groups), static_cast<unsigned>(a.max_parts),
-              static_cast<unsigned>(a.num_seqs));
+    const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
+    const dim3 grid = a.plan ? dim3(nh * static_cast<unsigned>(a.plan_capacity))
+                             : dim3(nh, static_cast<unsigned>(a.max_parts), static_cast<unsigned>(a.num_seqs));
     kern<<<grid, Geo<D, CW>::kThreads, smem, s>>>(tmk, tmv, a);
     return cudaGetLastError();
 }
@@ -313,8 +341,8 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_
     const int64_t nh = static_cast<int64_t>(num_kv_heads) * ((group + 7) / 8);
     const int parts = max_parts > 1 ? max_parts : 1;
     DecodeWorkspace w;
-    w.ticket_bytes = pad(sizeof(unsigned) * (2 + static_cast<size_t>(num_seqs) * nh));
-    w.item_bytes = pad(sizeof(unsigned) * static_cast<size_t>(num_seqs) * parts);
+    w.ticket_bytes = pad(sizeof(unsigned) * static_cast<size_t>(num_seqs) * nh);
+    w.plan_bytes = pad(sizeof(int4) * static_cast<size_t>(num_seqs) * parts);
     const size_t sh = static_cast<size_t>(num_seqs) * num_heads * (max_parts > 1 ? max_parts : 0);
     w.o_bytes = pad(sh * head_dim * sizeof(float));
     w.ml_bytes = pad(sh * 2 * sizeof(float));
@@ -350,14 +378,17 @@ int decode_ctas_per_sm(int head_dim) {
     return cache[i];
 }
 
-cudaError_t launch_decode_grid(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                               int head_dim, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                          int head_dim, cudaStream_t s) {
     if (a.num_seqs <= 0) return cudaSuccess;
-    if (a.max_parts > 1) {
+    cudaError_t e = cudaSuccess;
+    if (a.plan) {
+        e = launch_decode_plan(a, s);
+    } else if (a.max_parts > 1) {
         const size_t n = sizeof(unsigned) * static_cast<size_t>(a.num_seqs) * a.num_kv_heads * a.head_groups;
-        cudaError_t e = cudaMemsetAsync(a.tickets, 0, n, s);
-        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(a.tickets, 0, n, s);
     }
+    if (e != cudaSuccess) return e;
     const int st = ring_stages(), cw = consumer_warps();
     if (dtype == 0) {
         return head_dim == 128 ? launch_cfg<__half, 128>(a, tmk, tmv, cw, st, s)
@@ -365,18 +396,6 @@ cudaError_t launch_decode_grid(const DecodeArgs& a, const CUtensorMap& tmk, cons
     }
     return head_dim == 128 ? launch_cfg<__nv_bfloat16, 128>(a, tmk, tmv, cw, st, s)
                            : launch_cfg<__nv_bfloat16, 64>(a, tmk, tmv, cw, st, s);
-}
-
-// Variant: the grid kernel unless PKV_DECODE_VARIANT=persistent (read once).
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, cudaStream_t s) {
-    static const bool persistent = [] {
-        const char* e = getenv("PKV_DECODE_VARIANT");
-        return e && e[0] == 'p';
-    }();
-    // the persistent kernel serves one query token per sequence
-    return persistent && a.num_queries == 1 ? launch_decode_persistent(a, tmk, tmv, dtype, head_dim, s)
-                                            : launch_decode_grid(a, tmk, tmv, dtype, head_dim, s);
 }
 
 }  // namespace pkv

@@ -1,7 +1,6 @@
-// Pieces shared by the two decode kernels (grid and persistent): the shared
-// memory geometry of a chunk, the per-chunk consumer arithmetic and the
-// epilogue that merges warps and partitions.  Both kernels therefore compute
-// bit-identical results for the same partition size.
+// Pieces of the decode kernel: the shared memory geometry of a chunk, the
+// per-chunk consumer arithmetic and the epilogue that merges warps and
+// partitions; MQ instantiates the multi-query (verify) form.
 #pragma once
 
 #include <float.h>

@@ -40,20 +40,20 @@ struct CopyArgs {
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
-    void* out;                       // [B][Hq][D]
-    const void* q;                   // [B][Hq][D]
+    void* out;                       // [B][nq][Hq][D]
+    const void* q;                   // [B][nq][Hq][D]
     const int32_t* block_tables;     // [B][max_blocks_per_seq]
     const int32_t* seq_lens;         // [B]
-    unsigned* work_counter;          // next work unit of the persistent variant (zeroed per call)
-    unsigned* n_items;               // items in `items` (written per call by the plan kernel)
+    int4* plan;                      // [plan_capacity] work list (sequence, partition, length, partition
+                                     // tokens), written per call by the plan kernel; nullptr: direct grid
     unsigned* tickets;               // [B][num_kv_heads * head_groups] finished partitions (zeroed per call)
-    unsigned* items;                 // [B * max_parts] (sequence << 9 | partition), largest first
-    float* ws_o;                     // [B][Hq][max_parts][D] unnormalised partial outputs
-    float2* ws_ml;                   // [B][Hq][max_parts] (running max in log2 units, sum)
+    float* ws_o;                     // [B][Hq*nq][max_parts][D] unnormalised partial outputs
+    float2* ws_ml;                   // [B][Hq*nq][max_parts] (running max in log2 units, sum)
     unsigned* err;
     int64_t num_blocks;
     int max_blocks_per_seq;
     int num_seqs;
+    int max_seq_len;
     int num_heads;
     int num_kv_heads;
     int group;                       // query rows per KV head: (num_heads / num_kv_heads) * num_queries
@@ -61,36 +61,40 @@ struct DecodeArgs {
     int num_queries;                 // query tokens per sequence (1 = decode; > 1 = verify, causal)
     int head_groups;                 // ceil(group / 8): groups of query rows per KV head
     int block_size;
-    int part_tokens;                 // tokens per partition (multiple of 64)
-    int max_parts;                   // ceil(max_seq_len / part_tokens)
+    int part_tokens;                 // tokens per partition (multiple of 64); with a plan, the smallest the
+                                     // plan kernel may use
+    int part_auto;                   // with a plan: 1 = the plan kernel picks the partition size (>= part_tokens)
+    int slots;                       // SMs x resident decode CTAs per SM (for the plan kernel's choice)
+    int max_parts;                   // ceil(max_seq_len / part_tokens): the partials' stride
+    int plan_capacity;               // num_seqs * max_parts: entries of `plan` (the grid's work slots)
     float scale_log2;                // scale * log2(e)
 };
 
+// Sequences a call plans (sorts and compacts) at most; larger batches run the
+// direct grid (one CTA per (KV head group, partition, sequence)).
+constexpr int kPlanMaxSeqs = 1024;
+
 // Workspace layout of one decode call:
-//   [work counter, item count, tickets | item list | partial outputs | (max, sum) pairs]
+//   [tickets | work list | partial outputs | (max, sum) pairs]
 // each region 256-byte aligned.  Every call re-initialises what it uses.
 struct DecodeWorkspace {
-    size_t ticket_bytes;   // work counter + item count + tickets, padded
-    size_t item_bytes;     // item list, padded
+    size_t ticket_bytes;   // tickets, padded
+    size_t plan_bytes;     // work list (16 bytes per entry), padded
     size_t o_bytes;        // partial outputs, padded (0 when max_parts == 1)
     size_t ml_bytes;       // (max, sum) pairs (0 when max_parts == 1)
-    size_t total() const { return ticket_bytes + item_bytes + o_bytes + ml_bytes; }
+    size_t total() const { return ticket_bytes + plan_bytes + o_bytes + ml_bytes; }
 };
 DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_parts);
 
-// dtype: 0 = f16, 1 = bf16.  Runs one decode call on stream `s`: either the
-// grid variant (one CTA per work item; a memset zeroes the tickets) or the
-// persistent variant (a plan kernel builds the item list, then CTAs resident
-// on every SM pull items).  Both merge split partitions in-kernel.
+// dtype: 0 = f16, 1 = bf16.  Runs one decode call on stream `s`: the plan
+// kernel (work list + tickets) or, for a batch above kPlanMaxSeqs, a ticket
+// memset; then the decode kernel, which merges split partitions in-kernel.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
                           int head_dim, cudaStream_t s);
-cudaError_t launch_decode_grid(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                               int head_dim, cudaStream_t s);
-cudaError_t launch_decode_persistent(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                                     int head_dim, cudaStream_t s);
+cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s);
 
-// CTAs of the decode kernel resident per SM on the current device (grid
-// variant, current configuration), or 0 if it cannot be queried.
+// CTAs of the decode kernel resident per SM on the current device (current
+// configuration), or 0 if it cannot be queried.
 int decode_ctas_per_sm(int head_dim);
 
 // Record `msg` as the calling thread's pkv_last_error() message and return `st`.

@@ -125,6 +125,64 @@ def test_block_size_and_placement_invariance():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
+# ---------------------------------------------------------------- the plan kernel and the full grid
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+def test_batch_above_plan_limit_runs_the_full_grid(partition_tokens):
+    """More sequences than the plan kernel lists: the full (head group, partition,
+    sequence) grid, whose CTAs past their sequence's end return at once."""
+    B = pkv.PLAN_MAX_SEQS + 77
+    wl = W.build(W.small_spec(num_seqs=B, num_heads=8, num_kv_heads=2, head_dim=64, seed=501,
+                              lens=("uniform", 0, 150), pool=("headroom", 0.1)))
+    step = DeviceStep(wl, partition_tokens=partition_tokens)
+    step.run()
+    torch.cuda.synchronize()
+    full_check(wl, step)
+    s = wl.spec
+    assert pkv.decode_plan_partition_tokens(step.workspace, B, s.num_heads, s.num_kv_heads) == -1
+
+
+def test_plan_partition_size_bounds():
+    """Automatic: at least the host's size, a multiple of 64, within the staged
+    table, and no larger than the longest sequence needs; explicit: unchanged."""
+    wl = W.build(W.small_spec(num_seqs=6, num_heads=32, num_kv_heads=8, dtype=W.BF16, seed=502,
+                              lens=("fixed", (5000, 3000, 64, 1, 2100, 700))))
+    s = wl.spec
+    for p in (0, 192):
+        step = DeviceStep(wl, partition_tokens=p)
+        step.run()
+        got = pkv.decode_plan_partition_tokens(step.workspace, s.num_seqs, s.num_heads, s.num_kv_heads)
+        if p:
+            assert got == p
+        else:
+            lo = pkv.decode_partition_tokens(s.num_seqs, s.num_heads, s.num_kv_heads, s.head_dim, wl.max_seq_len)
+            assert got % 64 == 0 and lo <= got <= max(lo, 512 * s.block_size, -(-int(wl.seq_lens.max()) // 64) * 64)
+        torch.cuda.synchronize()
+        full_check(wl, step)
+
+
+@pytest.mark.parametrize("num_seqs", [5, pkv.PLAN_MAX_SEQS + 3])
+def test_lengths_above_max_seq_len_are_clamped_and_flagged(num_seqs):
+    """A length above max_seq_len breaks the call's precondition: the call attends
+    over max_seq_len positions and raises the bounds bit (planned and full grid)."""
+    rng = np.random.default_rng(503)
+    lens = rng.integers(1, 300, size=num_seqs)
+    lens[:3] = (299, 150, 40)
+    wl = W.build(W.small_spec(num_seqs=num_seqs, num_heads=8, num_kv_heads=2, head_dim=64, seed=504,
+                              lens=("fixed", tuple(int(x) for x in lens)), pool=("headroom", 0.1)))
+    step = DeviceStep(wl)
+    pkv.paged_kv_append(step.k_new, step.v_new, step.kc[0], step.vc[0], step.slot_mapping)
+    cap = 100
+    out = torch.full_like(step.q, float("nan"))
+    pkv.paged_attention_decode(out, step.q, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
+                               max_seq_len=cap, partition_tokens=64)
+    torch.cuda.synchronize()
+    assert pkv.device_error(reset=True) & 1, "a length above max_seq_len must raise the bounds bit"
+    kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
+    ref = oracle.attention_ref(wl.q, kc, vc, wl.block_tables, np.minimum(wl.seq_lens, cap), wl.scale,
+                               wl.spec.num_kv_heads, wl.spec.dtype)
+    assert max_abs_err(out, ref) <= TOL[wl.spec.dtype]
+
+
 # ---------------------------------------------------------------- full-size workloads
 FULL = ["llama3_8b", "llama2_70b_mixed_bs16", "llama2_70b_mixed_bs32", "cow_fork", "cow_fork_partial"]
 
@@ -136,6 +194,10 @@ def test_full_size_workload(name):
     pre_k, pre_v = to_bits(step.kc[0]), to_bits(step.vc[0])
     step.run()
     torch.cuda.synchronize()
+    s = wl.spec
+    part = pkv.decode_plan_partition_tokens(step.workspace, s.num_seqs, s.num_heads, s.num_kv_heads)
+    assert part % 64 == 0 and part >= pkv.decode_partition_tokens(s.num_seqs, s.num_heads, s.num_kv_heads,
+                                                                   s.head_dim, wl.max_seq_len)
     kc, vc = oracle_caches_after_step(wl, pre_k, pre_v)
     assert np.array_equal(to_bits(step.kc[0]), kc)
     assert np.array_equal(to_bits(step.vc[0]), vc)
