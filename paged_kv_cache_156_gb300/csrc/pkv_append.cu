@@ -15,6 +15,9 @@ namespace {
 constexpr int kWarpsPerBlock = 4;
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendArgs a) {
+    // a following decode call's plan kernel may start launching; it waits for
+    // this grid to finish before it reads anything
+    launch_dependents();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= a.num_tokens) return;

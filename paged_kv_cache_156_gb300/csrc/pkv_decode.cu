@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    grid_dependency_wait();                         // the plan and the pools come from earlier kernels
     // Work item: from the plan (one entry per (sequence, partition), KV head
     // groups innermost in the 1-D grid) or, without one, the 3-D grid itself.
     int hh, part, s, P, Lp;
@@ -292,10 +293,18 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensor
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
-    const dim3 grid = a.plan ? dim3(nh * static_cast<unsigned>(a.plan_capacity))
-                             : dim3(nh, static_cast<unsigned>(a.max_parts), static_cast<unsigned>(a.num_seqs));
-    kern<<<grid, Geo<D, CW>::kThreads, smem, s>>>(tmk, tmv, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = a.plan ? dim3(nh * static_cast<unsigned>(a.plan_capacity))
+                         : dim3(nh, static_cast<unsigned>(a.max_parts), static_cast<unsigned>(a.num_seqs));
+    cfg.blockDim = dim3(Geo<D, CW>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];                    // may launch while the plan kernel runs (it waits for it)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
 }
 
 template <typename T, int D>

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
     const int nh = a.num_kv_heads * a.head_groups;
     int nb = 0;                                     // next reduction buffer
     auto next = [&]() { long long* b = buf[nb]; nb ^= 1; return b; };
+    launch_dependents();                            // the decode grid may launch now; it waits for this grid
+    grid_dependency_wait();                         // lengths and tables may come from the previous kernel
 
     // ---- this thread's sequence: length (clamped to [0, max_seq_len]) and first block
     int L = 0, b0 = -1;
@@ -190,9 +192,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
 
 cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s) {
     if (a.num_seqs <= 0 || a.num_seqs > kPlanMaxSeqs || !a.plan) return cudaErrorInvalidValue;
-    const unsigned blocks = static_cast<unsigned>((a.num_seqs + kRankSeqs - 1) / kRankSeqs);
-    plan_kernel<<<blocks, kPlanThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((a.num_seqs + kRankSeqs - 1) / kRankSeqs));
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, a);
 }
 
 }  // namespace pkv

@@ -24,6 +24,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before its predecessor in the stream has finished;
+// grid_dependency_wait() blocks until every prerequisite grid has completed
+// and its writes are visible (a no-op without one), so it precedes the first
+// global read.  launch_dependents() lets the next such kernel start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
