@@ -94,7 +94,7 @@ def load_peaks():
 
 def decode_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("pkv_decode.cu", "pkv_device.cuh"):
+    for name in ("pkv_decode.cu", "pkv_decode_common.cuh", "pkv_decode_plan.cu", "pkv_device.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_156_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
