@@ -47,8 +47,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    p.add_argument("--op", default="decode", choices=["decode", "swap"],
-                   help="decode: the decode step (default); swap: preemption swap-out/in of a quarter of the batch")
+    p.add_argument("--op", default="decode", choices=["decode", "swap", "verify"],
+                   help="decode: the decode step (default); swap: preemption swap-out/in of a quarter of the "
+                        "batch; verify: the multi-query (speculative verify) call")
+    p.add_argument("--num-queries", type=int, default=4, help="query tokens per sequence for --op verify")
     p.add_argument("--workload", default="llama3_8b", choices=sorted(W.SPECS))
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
@@ -498,6 +500,24 @@ def run_swap(args, rank, world, local):
     out_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
     in_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev]))
     step_bytes = 2 * nb * block_bytes
+    # the link's roofline: the copy engines moving the same bytes between one
+    # contiguous pinned buffer and one device buffer (cudaMemcpyAsync via torch)
+    hbuf = torch.empty(nb * block_bytes, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(nb * block_bytes, dtype=torch.uint8, device=dev)
+    ce = []
+    for i in range(max(3, args.warmup) + args.steps):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record()
+        hbuf.copy_(dbuf, non_blocking=True)
+        b.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        c.record()
+        if i >= max(3, args.warmup):
+            ce.append((a, b, c))
+    torch.cuda.synchronize()
+    ce_out = float(np.mean([a.elapsed_time(b) for a, b, _ in ce]))
+    ce_in = float(np.mean([b.elapsed_time(c) for _, b, c in ce]))
+    ce_gbs = 2 * nb * block_bytes / ((ce_out + ce_in) / 1e3) / 1e9
     if rank != 0:
         return None
     return {"metric": "swap_blocks: device <-> pinned host GB/s (swap-out then swap-in)",
@@ -508,7 +528,85 @@ def run_swap(args, rank, world, local):
                                             "bytes_per_direction": int(nb * block_bytes), "layers": layers},
             "swap_out_GBps": round(nb * block_bytes / (out_ms / 1e3) / 1e9, 2),
             "swap_in_GBps": round(nb * block_bytes / (in_ms / 1e3) / 1e9, 2),
+            "roofline": {"bound": "link", "achieved": round(step_bytes / ((out_ms + in_ms) / 1e3) / 1e9, 2),
+                         "peak": round(ce_gbs, 2), "peak_kind": "measured: copy engines, same bytes, contiguous",
+                         "unit": "GB/s", "frac": round(step_bytes / ((out_ms + in_ms) / 1e3) / 1e9 / ce_gbs, 4),
+                         "copy_engine_out_GBps": round(nb * block_bytes / (ce_out / 1e3) / 1e9, 2),
+                         "copy_engine_in_GBps": round(nb * block_bytes / (ce_in / 1e3) / 1e9, 2)},
             "gpu_launches": 2 * args.steps * ((layers + 63) // 64)}
+
+
+def run_verify(args, rank, world, local):
+    """The multi-query verify call: num_queries query tokens per sequence, causal
+    among themselves, over the workload's paged K/V (the last num_queries
+    positions of each sequence are the query tokens' own).  Bytes: K/V of every
+    valid position once, plus q and out."""
+    from paged_kv_cache_156_gb300 import _build
+
+    if local == 0:
+        _build.build()
+    barrier(world)
+    import paged_kv_cache_156_gb300 as pkv
+
+    pkv.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = W.SPECS[args.workload]
+    if spec.num_layers != 1:
+        raise SystemExit("--op verify runs single-layer workloads")
+    wl = W.build(spec, values="none")
+    tdt = torch.float16 if spec.dtype == W.F16 else torch.bfloat16
+    nq = args.num_queries
+    B, Hq, d = spec.num_seqs, spec.num_heads, spec.head_dim
+    g = torch.Generator(device=dev)
+    g.manual_seed(spec.seed)
+    q = torch.randn((B, nq, Hq, d), generator=g, device=dev, dtype=torch.float32).to(tdt)
+    out = torch.empty_like(q)
+    tables = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(np.maximum(wl.seq_lens, nq)).to(dev)
+    footprint = wl.pool_bytes_per_layer()
+    replicas = max(2, min(4, math.ceil(3 * L2_BYTES / footprint)))
+    pools = [W.device_pools(wl, 0, dev) for _ in range(replicas)]
+    k_new = torch.from_numpy(np.ascontiguousarray(wl.k_new).view(np.int16)).to(dev).view(tdt)
+    v_new = torch.from_numpy(np.ascontiguousarray(wl.v_new).view(np.int16)).to(dev).view(tdt)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    for k, v in pools:                               # the step's new tokens, so every position holds one
+        pkv.paged_kv_append(k_new, v_new, k, v, slots)
+    ws = pkv.alloc_workspace(B, Hq * nq, spec.num_kv_heads, d, wl.max_seq_len, args.partition_tokens, dev)
+    nbytes = algorithmic_bytes(wl)["decode_unique"] + 2 * B * (nq - 1) * Hq * d * spec.elem_bytes
+
+    def call(i):
+        k, v = pools[i % replicas]
+        pkv.paged_attention_verify(out, q, k, v, tables, lens, wl.scale, max_seq_len=wl.max_seq_len, workspace=ws,
+                                   partition_tokens=args.partition_tokens)
+
+    for i in range(max(3, args.warmup)):
+        call(i)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        call(i)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    assert pkv.device_error() == 0
+    part = pkv.decode_plan_partition_tokens(ws, B, Hq * nq, spec.num_kv_heads) if B <= pkv.PLAN_MAX_SEQS else -1
+    if rank != 0:
+        return None
+    gbs = world * nbytes * args.steps / (ms / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    return {"metric": "paged verify attention GB/s (K/V of valid positions + q/out)", "value": round(gbs, 2),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+            "config": {"workload": spec.name, "num_queries": nq, "partition_tokens": part,
+                       "l2": f"{replicas} rotating pool replicas"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": round(gbs / world / peak, 4)},
+            "gpu_launches": 2 * args.steps}
 
 
 def main():
@@ -518,6 +616,8 @@ def main():
         res = run_reference(args, rank, world)
     elif args.op == "swap":
         res = run_swap(args, rank, world, local)
+    elif args.op == "verify":
+        res = run_verify(args, rank, world, local)
     else:
         res = run_pkv(args, rank, world, local)
     if rank == 0 and res is not None:

@@ -154,6 +154,69 @@ def test_append_slot_examples():
     assert seen == [b for b in tA for _ in range(16)]
 
 
+def test_block_engine_ref_append_slot_examples():
+    """The reference block manager hands out the pages' append_slot slots (P2 §2.3)."""
+    g = _gold("block_mapping_examples.json")["append_slot"]
+    bs = g["block_size"]
+    for c in g["cases"]:
+        first = list(c["blocks"]) + ([c["new_block"]] if c["new_block"] is not None else [])
+        NB = max(first) + 4
+        order = first + [b for b in range(NB) if b not in first]
+        eng = oracle.BlockEngineRef(NB, bs, free_order=order)
+        assert eng.allocate(0, c["current_len"]) and eng.tables[0] == list(c["blocks"])
+        slots, pairs = eng.append_slots([0])
+        assert slots == [c["slot"]] and pairs == []
+        if c["new_block"] is not None:
+            assert eng.tables[0][-1] == c["new_block"]
+
+
+def test_block_engine_ref_invariants_under_random_operations():
+    """Every block is free or held, never both; a block's count is the number of
+    sequences holding it; a failed call changes nothing (P2 §2.3, §3.3; P4 §五)."""
+    rng = np.random.default_rng(9)
+    NB, bs = 24, 4
+    eng = oracle.BlockEngineRef(NB, bs, free_order=rng.permutation(NB))
+    live, nxt = [], 0
+
+    def check():
+        held = {}
+        for t in eng.tables.values():
+            for b in t:
+                held[b] = held.get(b, 0) + 1
+        free = list(eng.free_list)
+        assert len(set(free)) == len(free) and not set(free) & set(held)
+        assert len(free) + len(held) == NB
+        assert all(eng.ref[b] == n for b, n in held.items()) and all(eng.ref[b] == 0 for b in free)
+        for sid, t in eng.tables.items():
+            assert len(t) == oracle.num_logical_blocks(eng.lens[sid], bs)
+
+    for _ in range(400):
+        op = rng.integers(4)
+        if op == 0:
+            if eng.allocate(nxt, int(rng.integers(0, 13))):
+                live.append(nxt)
+            nxt += 1
+        elif op == 1 and live:
+            if eng.fork(live[int(rng.integers(len(live)))], nxt):
+                live.append(nxt)
+            nxt += 1
+        elif op == 2 and live:
+            sid = live.pop(int(rng.integers(len(live))))
+            assert eng.free(sid)
+        elif live:
+            pick = list(rng.choice(live, size=min(len(live), int(rng.integers(1, 4))), replace=False))
+            before = (list(eng.free_list), {k: list(v) for k, v in eng.tables.items()}, dict(eng.lens))
+            r = eng.append_slots([int(x) for x in pick])
+            if r is None:
+                assert (list(eng.free_list), eng.tables, eng.lens) == before
+            else:
+                slots, pairs = r
+                assert len(set(slots)) == len(slots)
+                for src, dst in pairs:
+                    assert eng.ref[dst] == 1 and src != dst
+        check()
+
+
 # ---------------------------------------------------------------- cache writes
 def _rand_pool(rng, NB, bs, Hkv, d, dtype=F16):
     return (bits(rng.standard_normal((NB, bs, Hkv, d)), dtype),
