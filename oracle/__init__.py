@@ -38,19 +38,80 @@ import numpy as np
 
 F16 = "f16"
 BF16 = "bf16"
+E4M3 = "e4m3"    # 8-bit KV cache elements (see ``e4m3_value``)
 
 
 # --------------------------------------------------------------------------
 # element decoding
 # --------------------------------------------------------------------------
 def decode_bits(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """fp16 / bf16 bit patterns (uint16) -> float64, exactly."""
+    """fp16 / bf16 bit patterns (uint16) or E4M3 codes (uint8) -> float64, exactly."""
+    if dtype == E4M3:
+        return e4m3_value(bits)
     bits = np.asarray(bits, dtype=np.uint16)
     if dtype == F16:
         return bits.view(np.float16).astype(np.float64)
     if dtype == BF16:
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     raise ValueError(dtype)
+
+
+# --------------------------------------------------------------------------
+# 8-bit KV cache elements (P3 §6.2: KV cache quantization, attention on
+# low-precision K/V).  The page names no format; the reading taken is the OCP
+# FP8 E4M3 format ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3
+# mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448.  A
+# per-KV-head scale multiplies the decoded element.
+# --------------------------------------------------------------------------
+def e4m3_value(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) -> float64, exactly, from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    out = sign * mag
+    return np.where((e == 15) & ((c & 7) == 7), np.nan, out)
+
+
+_E4M3_POS = e4m3_value(np.arange(0x7F, dtype=np.uint8))     # codes 0x00..0x7E: 0 .. 448, increasing
+
+
+def e4m3_quantize(x: np.ndarray) -> np.ndarray:
+    """float32 values -> E4M3 codes: round to nearest, ties to the even code;
+    magnitudes above 448 (and infinities) become 448; NaN becomes 0x7F; the
+    sign is kept, so tiny negatives give -0 (0x80)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 1, 0x7E)   # first grid value >= a
+    lo = hi - 1
+    dlo = a - _E4M3_POS[lo]
+    dhi = _E4M3_POS[hi] - a
+    code = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a >= 448.0, 0x7E, code)
+    code = np.where(a == 0.0, 0, code)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    return np.where(np.isnan(x), 0x7F, code).astype(np.uint8)
+
+
+def append_fp8_ref(key_cache: np.ndarray, value_cache: np.ndarray, k: np.ndarray, v: np.ndarray,
+                   slot_mapping: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray, dtype: str) -> None:
+    """Quantize each new token's K/V rows into its slot of an E4M3 pool.
+
+    As ``append_ref`` (P2 §2.3 slot, P1 §4.2.2), with element (t, h, i) stored
+    as e4m3_quantize(float32(k[t, h, i]) / float32(k_scale[h])): the division
+    in float32, as the kernel does it.  Caches are uint8 [NB, bs, Hkv, d];
+    k, v are fp16 / bf16 bits [T, Hkv, d]; scales float32 [Hkv].
+    """
+    bs = key_cache.shape[1]
+    ks = np.asarray(k_scale, dtype=np.float32)[:, None]
+    vs = np.asarray(v_scale, dtype=np.float32)[:, None]
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        b, o = physical_location(int(slot), bs)
+        key_cache[b, o] = e4m3_quantize(decode_bits(k[t], dtype).astype(np.float32) / ks)
+        value_cache[b, o] = e4m3_quantize(decode_bits(v[t], dtype).astype(np.float32) / vs)
 
 
 # --------------------------------------------------------------------------
@@ -194,6 +255,30 @@ def attention_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
             V = gather_sequence(value_cache, block_tables[s], L, g, dtype)
             for h in range(g * G, (g + 1) * G):
                 out[s, h] = softmax_attention(decode_bits(q[s, h], dtype), K, V, scale)
+    return out
+
+
+def attention_fp8_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                      block_tables: np.ndarray, seq_lens: np.ndarray, scale: float, num_kv_heads: int,
+                      q_dtype: str, k_scale: np.ndarray, v_scale: np.ndarray) -> np.ndarray:
+    """Paged single-query attention over an E4M3 pool; float64 [B, num_heads, head_dim].
+
+    As ``attention_ref`` (P4 §2.2) with K_t = e4m3_value(code) * k_scale[g] and
+    V_t = e4m3_value(code) * v_scale[g] for KV head g (P3 §6.2: attention on
+    the low-precision K/V).  q: fp16 / bf16 bits [B, Hq, d]; caches uint8.
+    """
+    B, Hq, d = q.shape
+    G = Hq // num_kv_heads
+    ks = np.asarray(k_scale, dtype=np.float32).astype(np.float64)
+    vs = np.asarray(v_scale, dtype=np.float32).astype(np.float64)
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    for s in range(B):
+        L = int(seq_lens[s])
+        for g in range(num_kv_heads):
+            K = gather_sequence(key_cache, block_tables[s], L, g, E4M3) * ks[g]
+            V = gather_sequence(value_cache, block_tables[s], L, g, E4M3) * vs[g]
+            for h in range(g * G, (g + 1) * G):
+                out[s, h] = softmax_attention(decode_bits(q[s, h], q_dtype), K, V, scale)
     return out
 
 

@@ -84,3 +84,14 @@ def test_bf16_rounding_is_nearest_even():
     got = W.f32_to_bits(x, W.BF16)
     # ties go to even mantissa: 1+2^-8 -> 1.0 ; 1+3*2^-8 -> 1+2^-6 ; -1-2^-9 -> -1.0
     assert got.tolist() == [0x3F80, 0x3F82, 0xBF80, 0x4040]
+
+
+def test_e4m3_pools_finite_where_valid_and_poisoned_elsewhere():
+    wl = W.build(W.small_spec(kv_dtype=W.E4M3, lens=("fixed", (5, 40, 17, 1)), num_seqs=4))
+    for kc in (wl.key_caches[0], wl.value_caches[0]):
+        assert kc.dtype == np.uint8
+        vals = kc[wl.valid_slots]
+        assert not np.any((vals & 0x7F) == W.E4M3_NAN)           # no NaN code in a slot that holds a token
+        assert np.all(kc[~wl.valid_slots] == W.E4M3_NAN)
+    assert len(wl.k_scales) == 1 and wl.k_scales[0].dtype == np.float32 and np.all(wl.k_scales[0] > 0)
+    assert wl.pool_bytes_per_layer() == 2 * int(np.prod(wl.pool_shape()))

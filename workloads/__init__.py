@@ -13,7 +13,10 @@ What it builds, per workload:
                                  kernel may dereference.
 * pools             uint16 bit patterns [NB, bs, Hkv, d] of fp16 / bf16, one K
                                  and one V pool per layer.  Slots that hold no
-                                 token before the step are NaN.
+                                 token before the step are NaN.  An 8-bit
+                                 (E4M3) pool holds uint8 codes drawn at random
+                                 over a few binades, with per-layer, per-KV-head
+                                 float32 scales (``k_scales`` / ``v_scales``).
 * ``q``             [B, Hq, d];  ``k_new`` / ``v_new`` [T, Hkv, d] with
   ``slot_mapping`` int64 [T] (slot < 0: padding entry, nothing is written).
 * ``copy_pairs``    int64 [Np, 2] (src, dst) copy-on-write pairs for a fork.
@@ -34,9 +37,11 @@ import numpy as np
 
 F16 = "f16"
 BF16 = "bf16"
+E4M3 = "e4m3"
 DTYPES = (F16, BF16)
 # quiet-NaN bit patterns used to poison slots that hold no token
 NAN_BITS = {F16: 0x7E00, BF16: 0x7FC0}
+E4M3_NAN = 0x7F
 INT32_MAX = np.iinfo(np.int32).max
 
 
@@ -53,6 +58,17 @@ def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
         lsb = (u >> np.uint32(16)) & np.uint32(1)
         return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
     raise ValueError(dtype)
+
+
+def random_e4m3_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Random finite 8-bit E4M3 codes: random sign, exponent field 4..9
+    (magnitudes 2^-3 .. 7.5), random mantissa.  Arbitrary cache bytes, not a
+    quantization of anything."""
+    n = int(np.prod(shape))
+    sign = rng.integers(0, 2, n, dtype=np.uint8) << 7
+    exp = rng.integers(4, 10, n, dtype=np.uint8) << 3
+    man = rng.integers(0, 8, n, dtype=np.uint8)
+    return (sign | exp | man).reshape(shape)
 
 
 def normal_bits(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 24) -> np.ndarray:
@@ -83,6 +99,7 @@ class Spec:
     num_layers: int = 1
     fork: tuple | None = None         # (requests, n, prefix_len, suffix_lo, suffix_hi)
     description: str = ""
+    kv_dtype: str = ""                # "" = the pool holds `dtype`; E4M3 = 8-bit codes with scales
 
     @property
     def group(self) -> int:
@@ -90,7 +107,17 @@ class Spec:
 
     @property
     def elem_bytes(self) -> int:
+        """Bytes of a q / out / new K-V element (fp16 or bf16)."""
         return 2
+
+    @property
+    def fp8(self) -> bool:
+        return self.kv_dtype == E4M3
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        """Bytes of a pool element."""
+        return 1 if self.fp8 else 2
 
 
 SPECS = {
@@ -100,6 +127,9 @@ SPECS = {
     "llama3_8b": Spec(
         "llama3_8b", 64, 32, 8, 128, 16, BF16, 1002, ("uniform", 512, 4096),
         description="Llama-3-8B-shaped layer: 64 seqs U[512,4096], 32 q / 8 kv heads, d128, bs16, bf16, pool +20%"),
+    "llama3_8b_fp8": Spec(
+        "llama3_8b_fp8", 64, 32, 8, 128, 16, BF16, 1006, ("uniform", 512, 4096), kv_dtype=E4M3,
+        description="as llama3_8b with an 8-bit E4M3 K/V pool (per-KV-head scales), bf16 q and out"),
     "llama2_70b_mixed_bs16": Spec(
         "llama2_70b_mixed_bs16", 128, 64, 8, 128, 16, F16, 1003, ("lognormal", 500.0, 1.2, 32, 8192),
         description="Llama-2-70B-shaped layer: 128 seqs lognormal(500,1.2) in [32,8192], 64 q / 8 kv, d128, bs16, fp16"),
@@ -170,9 +200,11 @@ class Workload:
     slot_mapping: np.ndarray        # int64 [T]
     copy_pairs: np.ndarray          # int64 [Np, 2]
     valid_slots: np.ndarray         # bool [NB, bs]: slots holding a token before the step
-    key_caches: list = field(default_factory=list)    # per layer uint16 [NB, bs, Hkv, d] (host values)
+    key_caches: list = field(default_factory=list)    # per layer uint16 (uint8 for E4M3) [NB, bs, Hkv, d]
     value_caches: list = field(default_factory=list)
     layer_seeds: list = field(default_factory=list)
+    k_scales: list = field(default_factory=list)      # per layer float32 [Hkv] (E4M3 pools only)
+    v_scales: list = field(default_factory=list)
 
     @property
     def scale(self) -> float:
@@ -192,7 +224,7 @@ class Workload:
 
     def pool_bytes_per_layer(self) -> int:
         """Bytes of one layer's K pool plus V pool."""
-        return 2 * int(np.prod(self.pool_shape())) * self.spec.elem_bytes
+        return 2 * int(np.prod(self.pool_shape())) * self.spec.kv_elem_bytes
 
 
 def _draw_lens(spec: Spec, rng: np.random.Generator) -> np.ndarray:
@@ -314,12 +346,23 @@ def build(spec: Spec, values: str = "host") -> Workload:
                   q=q, k_new=k_new, v_new=v_new, slot_mapping=slot_mapping,
                   copy_pairs=np.asarray(cow_pairs, dtype=np.int64).reshape(-1, 2), valid_slots=valid)
     wl.layer_seeds = [int(spec.seed) * 1000 + l for l in range(spec.num_layers)]
+    if spec.fp8:
+        # per-KV-head scales of each layer, so dequantized codes are O(1)
+        srng = np.random.default_rng((spec.seed, 8))
+        for _ in range(spec.num_layers):
+            wl.k_scales.append(srng.uniform(0.05, 0.3, Hkv).astype(np.float32))
+            wl.v_scales.append(srng.uniform(0.05, 0.3, Hkv).astype(np.float32))
     if values == "host":
-        nan = np.uint16(NAN_BITS[spec.dtype])
         for l in range(spec.num_layers):
             lrng = np.random.default_rng(wl.layer_seeds[l])
-            kc = normal_bits(lrng, wl.pool_shape(), spec.dtype)
-            vc = normal_bits(lrng, wl.pool_shape(), spec.dtype)
+            if spec.fp8:
+                kc = random_e4m3_codes(lrng, wl.pool_shape())
+                vc = random_e4m3_codes(lrng, wl.pool_shape())
+                nan = np.uint8(E4M3_NAN)
+            else:
+                kc = normal_bits(lrng, wl.pool_shape(), spec.dtype)
+                vc = normal_bits(lrng, wl.pool_shape(), spec.dtype)
+                nan = np.uint16(NAN_BITS[spec.dtype])
             kc[~valid] = nan
             vc[~valid] = nan
             wl.key_caches.append(kc)
@@ -339,14 +382,22 @@ def device_pools(wl: Workload, layer: int, device="cuda"):
     import torch
 
     spec = wl.spec
-    tdt = torch.float16 if spec.dtype == F16 else torch.bfloat16
     g = torch.Generator(device=device)
     g.manual_seed(wl.layer_seeds[layer])
     mask = torch.from_numpy(~wl.valid_slots).to(device)
     out = []
     for _ in range(2):
-        x = torch.randn(wl.pool_shape(), generator=g, device=device, dtype=torch.float32).to(tdt)
-        x[mask] = float("nan")
+        if spec.fp8:                               # random finite E4M3 codes, as random_e4m3_codes
+            shape = wl.pool_shape()
+            sign = torch.randint(0, 2, shape, generator=g, device=device, dtype=torch.uint8) << 7
+            exp = torch.randint(4, 10, shape, generator=g, device=device, dtype=torch.uint8) << 3
+            man = torch.randint(0, 8, shape, generator=g, device=device, dtype=torch.uint8)
+            x = sign | exp | man
+            x[mask] = E4M3_NAN
+        else:
+            tdt = torch.float16 if spec.dtype == F16 else torch.bfloat16
+            x = torch.randn(wl.pool_shape(), generator=g, device=device, dtype=torch.float32).to(tdt)
+            x[mask] = float("nan")
         out.append(x)
     return out[0], out[1]
 
@@ -359,17 +410,22 @@ def host_pools_for(wl: Workload, seqs, layer: int = 0):
     contents do not depend on which sample asked for it.
     """
     spec = wl.spec
-    nan = np.uint16(NAN_BITS[spec.dtype])
-    kc = np.full(wl.pool_shape(), nan, dtype=np.uint16)
-    vc = np.full(wl.pool_shape(), nan, dtype=np.uint16)
+    if spec.fp8:
+        nan, store = np.uint8(E4M3_NAN), np.uint8
+        draw = lambda rng, shape: random_e4m3_codes(rng, shape)
+    else:
+        nan, store = np.uint16(NAN_BITS[spec.dtype]), np.uint16
+        draw = lambda rng, shape: normal_bits(rng, shape, spec.dtype)
+    kc = np.full(wl.pool_shape(), nan, dtype=store)
+    vc = np.full(wl.pool_shape(), nan, dtype=store)
     blk_shape = wl.pool_shape()[1:]
     for s in seqs:
         nb = blocks_needed(int(wl.seq_lens[s]), spec.block_size)
         for b in wl.block_tables[s, :nb]:
             b = int(b)
             rng = np.random.default_rng((wl.layer_seeds[layer], b))
-            kc[b] = normal_bits(rng, blk_shape, spec.dtype)
-            vc[b] = normal_bits(rng, blk_shape, spec.dtype)
+            kc[b] = draw(rng, blk_shape)
+            vc[b] = draw(rng, blk_shape)
             kc[b][~wl.valid_slots[b]] = nan
             vc[b][~wl.valid_slots[b]] = nan
     return kc, vc
