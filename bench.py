@@ -21,6 +21,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
+import functools
 import hashlib
 import json
 import math
@@ -66,20 +67,21 @@ def algorithmic_bytes(wl: W.Workload) -> dict:
     """Algorithmic bytes of one step (one replica)."""
     s = wl.spec
     e, Hkv, Hq, d, bs = s.elem_bytes, s.num_kv_heads, s.num_heads, s.head_dim, s.block_size
+    ekv = s.kv_elem_bytes                                  # 1 for an E4M3 pool
     L = wl.seq_lens.astype(np.int64)
     nb = (L + bs - 1) // bs
     small = 2 * s.num_seqs * Hq * d * e + 4 * int(nb.sum()) + 4 * s.num_seqs
-    logical = int(2 * L.sum() * Hkv * d * e) + small
+    logical = int(2 * L.sum() * Hkv * d * ekv) + small
     # unique: each physical (block, slot) read once even if several sequences share it
     seen = {}
     for i in range(s.num_seqs):
         for j in range(int(nb[i])):
             b = int(wl.block_tables[i, j])
             seen[b] = max(seen.get(b, 0), min(bs, int(L[i]) - j * bs))
-    unique = int(2 * sum(seen.values()) * Hkv * d * e) + small
+    unique = int(2 * sum(seen.values()) * Hkv * d * ekv) + small
     valid_tok = int((wl.slot_mapping >= 0).sum())
-    append = 2 * 2 * valid_tok * Hkv * d * e + 8 * wl.num_tokens
-    copy = 2 * 2 * len(wl.copy_pairs) * bs * Hkv * d * e * s.num_layers
+    append = 2 * valid_tok * Hkv * d * (e + ekv) + 8 * wl.num_tokens + (8 * Hkv if s.fp8 else 0)
+    copy = 2 * 2 * len(wl.copy_pairs) * bs * Hkv * d * ekv * s.num_layers
     step = copy + s.num_layers * (append + unique)
     return dict(decode_unique=unique, decode_logical=logical, append=append, copy=copy, step=step)
 
@@ -170,19 +172,25 @@ def time_oracle(wl: W.Workload, pools, seqs, budget_s: float):
         tok_of[s] = list(range(t, t + n))
         t += n
     per = algorithmic_bytes(wl)
-    Hkv, d, e = spec.num_kv_heads, spec.head_dim, spec.elem_bytes
+    Hkv, d, e, ekv = spec.num_kv_heads, spec.head_dim, spec.elem_bytes, spec.kv_elem_bytes
     done_bytes, done = 0, 0
     t0 = time.perf_counter()
     i = 0
     while True:
         s = seqs[i % len(seqs)]
         idx = tok_of[s]
-        oracle.append_ref(kc, vc, wl.k_new[idx], wl.v_new[idx], wl.slot_mapping[idx])
-        oracle.attention_ref(wl.q[s:s + 1], kc, vc, wl.block_tables[s:s + 1], wl.seq_lens[s:s + 1], wl.scale, Hkv,
-                             spec.dtype)
+        if spec.fp8:
+            ks, vs = wl.k_scales[0], wl.v_scales[0]
+            oracle.append_fp8_ref(kc, vc, wl.k_new[idx], wl.v_new[idx], wl.slot_mapping[idx], ks, vs, spec.dtype)
+            oracle.attention_fp8_ref(wl.q[s:s + 1], kc, vc, wl.block_tables[s:s + 1], wl.seq_lens[s:s + 1], wl.scale,
+                                     Hkv, spec.dtype, ks, vs)
+        else:
+            oracle.append_ref(kc, vc, wl.k_new[idx], wl.v_new[idx], wl.slot_mapping[idx])
+            oracle.attention_ref(wl.q[s:s + 1], kc, vc, wl.block_tables[s:s + 1], wl.seq_lens[s:s + 1], wl.scale, Hkv,
+                                 spec.dtype)
         L = int(wl.seq_lens[s])
-        done_bytes += 2 * L * Hkv * d * e + 2 * spec.num_heads * d * e + 4 * W.blocks_needed(L, spec.block_size) + 4
-        done_bytes += 4 * len(idx) * Hkv * d * e + 8 * len(idx)
+        done_bytes += 2 * L * Hkv * d * ekv + 2 * spec.num_heads * d * e + 4 * W.blocks_needed(L, spec.block_size) + 4
+        done_bytes += 2 * len(idx) * Hkv * d * (e + ekv) + 8 * len(idx)
         done += 1
         i += 1
         if time.perf_counter() - t0 >= budget_s:
@@ -266,6 +274,8 @@ def run_pkv(args, rank, world, local):
             vcs.append(v)
         pools.append((kcs, vcs))
     outs = [torch.empty_like(q) for _ in range(spec.num_layers)]
+    k_scales = [torch.from_numpy(x).to(dev) for x in wl.k_scales]      # E4M3 pools only
+    v_scales = [torch.from_numpy(x).to(dev) for x in wl.v_scales]
     # 0 = automatic: the host sizes the workspace for the smallest partition,
     # the plan kernel picks the size from the lengths
     part_min = args.partition_tokens or pkv.decode_partition_tokens(spec.num_seqs, spec.num_heads,
@@ -285,14 +295,18 @@ def run_pkv(args, rank, world, local):
         if len(wl.copy_pairs):
             pkv.copy_blocks(kcs, vcs, pairs)
         for l in range(spec.num_layers):
-            pkv.paged_kv_append(k_new, v_new, kcs[l], vcs[l], slots)
+            if spec.fp8:
+                pkv.paged_kv_append_fp8(k_new, v_new, kcs[l], vcs[l], slots, k_scales[l], v_scales[l])
+            else:
+                pkv.paged_kv_append(k_new, v_new, kcs[l], vcs[l], slots)
             rec = timed and l == 0
             if rec:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
-            pkv.paged_attention_decode(outs[l], q, kcs[l], vcs[l], tables, lens, wl.scale,
-                                       max_seq_len=wl.max_seq_len, workspace=ws,
-                                       partition_tokens=args.partition_tokens)
+            decode = (functools.partial(pkv.paged_attention_decode_fp8, k_scale=k_scales[l], v_scale=v_scales[l])
+                      if spec.fp8 else pkv.paged_attention_decode)
+            decode(outs[l], q, kcs[l], vcs[l], tables, lens, scale=wl.scale, max_seq_len=wl.max_seq_len,
+                   workspace=ws, partition_tokens=args.partition_tokens)
             if rec:
                 b.record()
                 ev_pairs.append((a, b))
@@ -355,8 +369,12 @@ def run_pkv(args, rank, world, local):
     # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        kc0 = pools[0][0][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).copy()
-        vc0 = pools[0][1][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).copy()
+        if spec.fp8:
+            kc0 = pools[0][0][0].cpu().numpy().copy()
+            vc0 = pools[0][1][0].cpu().numpy().copy()
+        else:
+            kc0 = pools[0][0][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).copy()
+            vc0 = pools[0][1][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).copy()
         seqs = sample_for_oracle(wl)
         b, sec, n = time_oracle(wl, (kc0, vc0), seqs, args.cpu_seconds)
         cpu = {"value": round(b / sec / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -382,6 +400,7 @@ def run_pkv(args, rank, world, local):
         "config": {"workload": spec.name, "description": spec.description, "num_seqs": spec.num_seqs,
                    "num_heads": spec.num_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
                    "block_size": spec.block_size, "num_layers": spec.num_layers,
+                   "kv_dtype": spec.kv_dtype or spec.dtype,
                    "mean_seq_len": round(float(wl.seq_lens.mean()), 1), "max_seq_len": wl.max_seq_len,
                    "num_blocks": wl.num_blocks, "copy_pairs": int(len(wl.copy_pairs)),
                    "partition_tokens": part, "partition_tokens_min": part_min, "max_partitions": max_parts,

@@ -59,7 +59,10 @@ typedef enum {
     PKV_ERR_OOM = 5           /* block manager: not enough free blocks (nothing changed) */
 } pkv_status;
 
-typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* Element types.  PKV_E4M3 (8-bit OCP FP8 E4M3 codes) is a pool type only:
+ * accepted by pkv_copy_blocks / pkv_swap_blocks and as the pool of the
+ * *_fp8 calls, never for q, out or new K/V. */
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_E4M3 = 2 } pkv_dtype;
 
 /* Library ABI version (major * 100 + minor). */
 PKV_API int pkv_version(void);
@@ -202,6 +205,44 @@ PKV_API pkv_status pkv_paged_attention_verify(void* out, const void* q, const vo
                                       int partition_tokens, void* stream);
 
 /*
+ * 8-bit KV cache (E4M3) -- P3 §6.2 (KV cache quantization: attention reads
+ * low-precision K/V, saving memory and bandwidth with little accuracy loss).
+ * The page names no format; these calls use OCP FP8 E4M3 codes (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, largest finite 448, no
+ * infinities) with one float32 scale per KV head for K and one for V: the
+ * element a code stands for is e4m3_value(code) * scale[kv_head].
+ *
+ * pkv_paged_kv_append_fp8: as pkv_paged_kv_append into uint8 pools; element
+ * (t, h, i) becomes e4m3(float32(k[t][h][i]) / k_scale[h]) (IEEE division,
+ * round to nearest even, magnitudes above 448 saturate to 448, NaN stays
+ * NaN); likewise V with v_scale.
+ *   k, v              [T][num_kv_heads][head_dim] fp16 / bf16 (`dt`), 16-byte aligned
+ *   key_cache,
+ *   value_cache       uint8 [num_blocks][block_size][num_kv_heads][head_dim], 8-byte aligned
+ *   k_scale, v_scale  device float32 [num_kv_heads], each > 0 (not checked)
+ */
+PKV_API pkv_status pkv_paged_kv_append_fp8(const void* k, const void* v, void* key_cache, void* value_cache,
+                                   const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                                   int block_size, int num_kv_heads, int head_dim, pkv_dtype dt,
+                                   const float* k_scale, const float* v_scale, void* stream);
+
+/*
+ * pkv_paged_attention_decode_fp8: pkv_paged_attention_decode over uint8 E4M3
+ * pools, K_t = e4m3_value(code) * k_scale[g] and V_t = e4m3_value(code) *
+ * v_scale[g] for KV head g; q and out are fp16 / bf16 (`dt`).  Same
+ * workspace, partitioning and plan.  head_dim 128 only.  The tensor cores
+ * run in f16: every E4M3 value is exact in f16, and q is converted to f16
+ * (exact for |q| < 65504; a bf16 query beyond f16's range is not supported).
+ */
+PKV_API pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* key_cache,
+                                          const void* value_cache, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                          int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                          const float* k_scale, const float* v_scale, void* workspace,
+                                          size_t workspace_bytes, int partition_tokens, void* stream);
+
+/*
  * copy_blocks -- the copy-on-write block copy at a fork.
  *
  * P2 §3.1 (the scheduler output's blocks_to_copy, "用于 Copy-on-Write") and
@@ -213,6 +254,7 @@ PKV_API pkv_status pkv_paged_attention_verify(void* out, const void* q, const vo
  *   key_caches, value_caches  HOST arrays of num_layers device pointers, each a
  *                             pool [num_blocks][block_size][num_kv_heads][head_dim]
  *   src_dst_pairs             DEVICE int64 [num_pairs][2]
+ *   dt                        the pools' element type (PKV_F16, PKV_BF16 or PKV_E4M3)
  * Destinations must be distinct and must not appear as a source (the pairs
  * are applied concurrently).  num_pairs == 0 or num_layers == 0 is a no-op.
  */

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
 
 PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_OOM = range(6)
 _DT = {torch.float16: 0, torch.bfloat16: 1}
+_POOL_DT = {torch.float16: 0, torch.bfloat16: 1, torch.uint8: 2}   # uint8 pools hold E4M3 codes
 PLAN_MAX_SEQS = 1024        # PKV_PLAN_MAX_SEQS: batches up to this size run through the plan kernel
 
 # every symbol include/pkv.h declares
@@ -29,7 +30,8 @@ ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_deco
                "pkv_decode_partition_tokens", "pkv_decode_plan_partition_tokens", "pkv_paged_attention_decode", "pkv_copy_blocks", "pkv_device_error",
                "pkv_paged_attention_decode_static", "pkv_swap_blocks", "pkv_paged_attention_verify", "pkv_bm_create", "pkv_bm_destroy",
                "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
-               "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables")
+               "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables", "pkv_paged_kv_append_fp8",
+               "pkv_paged_attention_decode_fp8")
 
 _lib = None
 
@@ -67,6 +69,11 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_verify.restype = c_i
     lib.pkv_paged_attention_verify.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                c_i64, c_f, c_i, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_paged_kv_append_fp8.restype = c_i
+    lib.pkv_paged_kv_append_fp8.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i, c_i, c_i, c_i, c_p, c_p, c_p]
+    lib.pkv_paged_attention_decode_fp8.restype = c_i
+    lib.pkv_paged_attention_decode_fp8.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
+                                                   c_i64, c_f, c_i, c_p, c_p, c_p, c_sz, c_i, c_p]
     lib.pkv_copy_blocks.restype = c_i
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p, c_i64, c_i64, c_i, c_i,
                                     c_i, c_i, c_p]
@@ -118,8 +125,8 @@ def _cuda(name, t, dtype=None, ndim=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _pool(name, c):
-    _cuda(name, c, (torch.float16, torch.bfloat16), 4)
+def _pool(name, c, dtypes=(torch.float16, torch.bfloat16)):
+    _cuda(name, c, dtypes, 4)
     return c.shape  # num_blocks, block_size, num_kv_heads, head_dim
 
 
@@ -196,6 +203,59 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_len
         NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
 
 
+def _scales(name, t, Hkv):
+    _cuda(name, t, torch.float32, 1)
+    if t.shape[0] != Hkv:
+        raise ValueError(f"{name} must have num_kv_heads = {Hkv} entries")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def paged_kv_append_fp8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_scale) -> None:
+    """Quantize k[t], v[t] ([T, Hkv, d], fp16 / bf16) into slot slot_mapping[t] of uint8 E4M3 pools:
+    code = e4m3(float32(x) / scale[head]) (nearest even, saturating); k_scale, v_scale float32 [Hkv]."""
+    NB, bs, Hkv, d = _pool("key_cache", key_cache, (torch.uint8,))
+    if value_cache.shape != key_cache.shape or value_cache.dtype != torch.uint8:
+        raise ValueError("value_cache must match key_cache")
+    T = k.shape[0]
+    if tuple(k.shape) != (T, Hkv, d) or v.shape != k.shape or v.dtype != k.dtype:
+        raise ValueError("k and v must be [T, num_kv_heads, head_dim] of one dtype")
+    args = [_cuda("k", k, (torch.float16, torch.bfloat16)), _cuda("v", v, k.dtype), _cuda("key_cache", key_cache),
+            _cuda("value_cache", value_cache), _cuda("slot_mapping", slot_mapping, torch.int64, 1)]
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have T entries")
+    _check(load().pkv_paged_kv_append_fp8(*args, T, NB, bs, Hkv, d, _DT[k.dtype], _scales("k_scale", k_scale, Hkv),
+                                          _scales("v_scale", v_scale, Hkv), _stream(key_cache)))
+
+
+def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq_lens, k_scale, v_scale, scale=None,
+                               max_seq_len=None, workspace=None, partition_tokens=0) -> None:
+    """paged_attention_decode over uint8 E4M3 pools: K = e4m3(code) * k_scale[g], V = e4m3(code) * v_scale[g];
+    q, out fp16 / bf16 [B, Hq, 128]; k_scale, v_scale float32 [Hkv]."""
+    NB, bs, Hkv, d = _pool("key_cache", key_cache, (torch.uint8,))
+    if value_cache.shape != key_cache.shape or value_cache.dtype != torch.uint8:
+        raise ValueError("value_cache must match key_cache")
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d):
+        raise ValueError("q and out must be [B, num_heads, head_dim]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    ptrs = [_cuda("out", out, (torch.float16, torch.bfloat16)), _cuda("q", q, out.dtype), _cuda("key_cache", key_cache),
+            _cuda("value_cache", value_cache), _cuda("block_tables", block_tables, torch.int32, 2)]
+    _cuda("seq_lens", seq_lens, torch.int32, 1)
+    if block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_tables / seq_lens batch mismatch")
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
+    ws_ptr = _cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_attention_decode_fp8(
+        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
+        NB, float(scale), _DT[q.dtype], _scales("k_scale", k_scale, Hkv), _scales("v_scale", v_scale, Hkv), ws_ptr,
+        ws_bytes, int(partition_tokens), _stream(q)))
+
+
 def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,
                            workspace=None, partition_tokens=0) -> None:
     """Multi-query paged attention: q, out [B, nq, Hq, d]; query token i of sequence s attends over
@@ -234,8 +294,8 @@ def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:
         raise ValueError("need the same non-zero number of key and value caches")
     shape, dt = key_caches[0].shape, key_caches[0].dtype
     for i, (kc, vc) in enumerate(zip(key_caches, value_caches)):
-        _pool(f"key_caches[{i}]", kc)
-        _pool(f"value_caches[{i}]", vc)
+        _pool(f"key_caches[{i}]", kc, tuple(_POOL_DT))
+        _pool(f"value_caches[{i}]", vc, tuple(_POOL_DT))
         if kc.shape != shape or vc.shape != shape or kc.dtype != dt or vc.dtype != dt:
             raise ValueError("all caches must share shape and dtype")
     _cuda("src_dst_pairs", src_dst_pairs, torch.int64, 2)
@@ -246,13 +306,13 @@ def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:
     varr = (ctypes.c_void_p * n)(*[vc.data_ptr() for vc in value_caches])
     NB, bs, Hkv, d = shape
     _check(load().pkv_copy_blocks(karr, varr, n, ctypes.c_void_p(src_dst_pairs.data_ptr()), src_dst_pairs.shape[0],
-                                  NB, bs, Hkv, d, _DT[dt], _stream(key_caches[0])))
+                                  NB, bs, Hkv, d, _POOL_DT[dt], _stream(key_caches[0])))
 
 
 def _addressable_pool(name, t):
     """A pool the GPU can address: a CUDA tensor or a pinned CPU tensor."""
-    if not isinstance(t, torch.Tensor) or t.dim() != 4 or t.dtype not in (torch.float16, torch.bfloat16):
-        raise ValueError(f"{name} must be a 4-D fp16/bf16 tensor")
+    if not isinstance(t, torch.Tensor) or t.dim() != 4 or t.dtype not in _POOL_DT:
+        raise ValueError(f"{name} must be a 4-D fp16 / bf16 / uint8 (E4M3) tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if not t.is_cuda and not t.is_pinned():
@@ -284,7 +344,7 @@ def swap_blocks(src_key_caches, src_value_caches, dst_key_caches, dst_value_cach
     arrs = [(ctypes.c_void_p * n)(*ptrs[k * n:(k + 1) * n]) for k in range(4)]
     _, bs, Hkv, d = src_shape
     _check(load().pkv_swap_blocks(*arrs, n, ctypes.c_void_p(src_dst_pairs.data_ptr()), src_dst_pairs.shape[0],
-                                  src_shape[0], dst_shape[0], bs, Hkv, d, _DT[dt], _stream(src_dst_pairs)))
+                                  src_shape[0], dst_shape[0], bs, Hkv, d, _POOL_DT[dt], _stream(src_dst_pairs)))
 
 
 class BlockManager:

@@ -85,19 +85,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // TMA descriptor of one pool [num_blocks][block_size][num_kv_heads][head_dim]
-// (16-bit elements).  One box is one (physical block, KV head) tile:
-// block_size rows of 64 elements (128 bytes), 128-byte swizzled in shared memory.
-pkv_status encode_pool(CUtensorMap* map, const void* base, int64_t num_blocks, int bs, int hkv, int d) {
+// of `e`-byte elements (2: fp16 / bf16; 1: E4M3 codes).  One box is one
+// (physical block, KV head) tile: block_size rows of 128 bytes (64 or 128
+// elements), 128-byte swizzled in shared memory.
+pkv_status encode_pool(CUtensorMap* map, const void* base, int64_t num_blocks, int bs, int hkv, int d, int e = 2) {
     auto enc = encode_fn();
     if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t e = 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(bs),
                           static_cast<cuuint64_t>(num_blocks)};
     cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(hkv) * d * e,
                              static_cast<cuuint64_t>(bs) * hkv * d * e};
-    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(bs), 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / e), 1, static_cast<cuuint32_t>(bs), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = enc(map, e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                     const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -251,9 +252,13 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
                           int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, pkv_dtype dt, int num_queries, void* workspace,
-                          size_t workspace_bytes, int partition_tokens, void* stream) {
+                          size_t workspace_bytes, int partition_tokens, void* stream, const float* k_scale = nullptr,
+                          const float* v_scale = nullptr) {
     pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
     if (st != PKV_OK) return st;
+    const bool kv8 = k_scale || v_scale;                  // an E4M3 pool (the _fp8 entry point)
+    if (kv8 && (head_dim != 128 || num_queries != 1))
+        return fail(PKV_ERR_UNSUPPORTED, "E4M3 pools: head_dim 128 and one query token only");
     if (num_queries < 1 || num_queries > 64) return fail(PKV_ERR_INVALID, "num_queries %d outside [1, 64]", num_queries);
     const int rows = num_heads * num_queries;            // query rows per sequence
     if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
@@ -267,8 +272,10 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     if (partition_tokens < 0 || partition_tokens > kMaxPartition || partition_tokens % kChunk != 0)
         return fail(PKV_ERR_INVALID, "partition_tokens %d: 0 or a multiple of 64 up to 4096", partition_tokens);
     if (num_seqs == 0) return ok();
-    if (!out || !q || !key_cache || !value_cache || !block_tables || !seq_lens)
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !seq_lens || (kv8 && (!k_scale || !v_scale)))
         return fail(PKV_ERR_INVALID, "null pointer");
+    if (kv8 && ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u)))
+        return fail(PKV_ERR_INVALID, "k_scale / v_scale must be 4-byte aligned");
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned; tables and lengths 4-byte");
@@ -290,8 +297,9 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
         return fail(PKV_ERR_UNSUPPORTED, "too many work items");
 
     CUtensorMap tmk, tmv;
-    if ((st = encode_pool(&tmk, key_cache, num_blocks, block_size, num_kv_heads, head_dim)) != PKV_OK) return st;
-    if ((st = encode_pool(&tmv, value_cache, num_blocks, block_size, num_kv_heads, head_dim)) != PKV_OK) return st;
+    const int eb = kv8 ? 1 : 2;
+    if ((st = encode_pool(&tmk, key_cache, num_blocks, block_size, num_kv_heads, head_dim, eb)) != PKV_OK) return st;
+    if ((st = encode_pool(&tmv, value_cache, num_blocks, block_size, num_kv_heads, head_dim, eb)) != PKV_OK) return st;
 
     pkv::DecodeArgs a;
     a.out = out;
@@ -317,11 +325,14 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.block_size = block_size;
     a.part_tokens = part;
     a.part_auto = partition_tokens == 0;
-    a.slots = sm_count_of(dev) * pkv::decode_ctas_per_sm(head_dim);
+    a.slots = sm_count_of(dev) * pkv::decode_ctas_per_sm(head_dim, kv8);
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
     a.plan_capacity = num_seqs * static_cast<int>(max_parts);
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.kv8 = kv8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
     return ok();
@@ -351,6 +362,55 @@ pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_
                           num_queries, workspace, workspace_bytes, partition_tokens, stream);
 }
 
+pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                          int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                          const float* k_scale, const float* v_scale, void* workspace,
+                                          size_t workspace_bytes, int partition_tokens, void* stream) {
+    if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "k_scale / v_scale are required");
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
+                          workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale);
+}
+
+pkv_status pkv_paged_kv_append_fp8(const void* k, const void* v, void* key_cache, void* value_cache,
+                                   const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks, int block_size,
+                                   int num_kv_heads, int head_dim, pkv_dtype dt, const float* k_scale,
+                                   const float* v_scale, void* stream) {
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID, "num_tokens %lld < 0", static_cast<long long>(num_tokens));
+    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d (fp16 or bf16 inputs)", static_cast<int>(dt));
+    if (num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0)
+        return fail(PKV_ERR_INVALID, "num_kv_heads %d / head_dim %d (head_dim must be a positive multiple of 8)",
+                    num_kv_heads, head_dim);
+    if (block_size <= 0 || num_blocks <= 0)
+        return fail(PKV_ERR_INVALID, "block_size %d / num_blocks %lld", block_size, static_cast<long long>(num_blocks));
+    if (num_tokens == 0) return ok();
+    if (!k || !v || !key_cache || !value_cache || !slot_mapping || !k_scale || !v_scale)
+        return fail(PKV_ERR_INVALID, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(key_cache) & 7u) ||
+        (reinterpret_cast<uintptr_t>(value_cache) & 7u) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+        (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return fail(PKV_ERR_INVALID, "k, v 16-byte aligned; caches and slot_mapping 8-byte; scales 4-byte");
+    pkv::AppendFp8Args a;
+    a.k = static_cast<const uint4*>(k);
+    a.v = static_cast<const uint4*>(v);
+    a.key_cache = static_cast<uint2*>(key_cache);
+    a.value_cache = static_cast<uint2*>(value_cache);
+    a.slots = slot_mapping;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.num_tokens = num_tokens;
+    a.num_slots = num_blocks * block_size;
+    a.row_vecs = num_kv_heads * head_dim / 8;
+    a.head_vecs = head_dim / 8;
+    a.bf16 = dt == PKV_BF16;
+    a.err = error_word(current_device());
+    cudaError_t e = pkv::launch_append_fp8(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 }  // extern "C"
 
 namespace {
@@ -361,10 +421,10 @@ pkv_status block_copies(void* const* src_key, void* const* src_value, void* cons
                         int64_t dst_num_blocks, int block_size, int num_kv_heads, int head_dim, pkv_dtype dt,
                         void* stream, const char* what) {
     if (num_layers < 0 || num_pairs < 0) return fail(PKV_ERR_INVALID, "%s: num_layers / num_pairs < 0", what);
-    if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "%s: dtype %d", what, static_cast<int>(dt));
+    if (!valid_dtype(dt) && dt != PKV_E4M3) return fail(PKV_ERR_UNSUPPORTED, "%s: dtype %d", what, static_cast<int>(dt));
     if (block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
         return fail(PKV_ERR_INVALID, "%s: bad pool shape", what);
-    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+    const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * (dt == PKV_E4M3 ? 1 : 2);
     if (block_bytes % 16 != 0)
         return fail(PKV_ERR_INVALID, "%s: block bytes %lld not a multiple of 16", what,
                     static_cast<long long>(block_bytes));

@@ -6,6 +6,9 @@
 // num_kv_heads * head_dim elements.  One warp moves one token: its K row and V
 // row are each num_kv_heads * head_dim * 2 contiguous bytes in both the input
 // and the pool, copied with 16-byte vector loads and stores.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -38,7 +41,66 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
         vd[i] = y;
     }
 }
+
+// ---------------------------------------------------------------- E4M3 pools
+// The same scatter into an 8-bit pool (the KV quantization of "LLM 推理优化深度实战"
+// §6.2: attention then reads low-precision K/V).  Each lane converts 8
+// elements per step: float32, divided by its KV head's scale (IEEE division),
+// rounded to the nearest E4M3 code (ties to even) with saturation at 448.
+template <bool BF16>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t x) {
+    if constexpr (BF16) return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+    else return __half22float2(*reinterpret_cast<const __half2*>(&x));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
+    uint32_t w[4];
+    const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = pair_to_float2<BF16>(in[i]);
+        w[i] = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale)), __NV_SATFINITE,
+                                        __NV_E4M3);
+    }
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_fp8_kernel(const AppendFp8Args a) {
+    launch_dependents();
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= a.num_tokens) return;
+    const int64_t slot = a.slots[t];
+    if (slot < 0) return;
+    if (slot >= a.num_slots) {
+        if (lane == 0) raise_error(a.err, kErrBounds);
+        return;
+    }
+    const uint4* ks = a.k + t * a.row_vecs;
+    const uint4* vs = a.v + t * a.row_vecs;
+    uint2* kd = a.key_cache + slot * a.row_vecs;
+    uint2* vd = a.value_cache + slot * a.row_vecs;
+    for (int i = lane; i < a.row_vecs; i += 32) {
+        const int h = i / a.head_vecs;
+        const uint4 x = __ldg(ks + i);
+        const uint4 y = __ldg(vs + i);
+        kd[i] = quantize8<BF16>(x, __ldg(a.k_scale + h));
+        vd[i] = quantize8<BF16>(y, __ldg(a.v_scale + h));
+    }
+}
 }  // namespace
+
+cudaError_t launch_append_fp8(const AppendFp8Args& a, cudaStream_t s) {
+    if (a.num_tokens <= 0) return cudaSuccess;
+    const int64_t blocks = (a.num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (a.bf16)
+        append_fp8_kernel<true><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, s>>>(a);
+    else
+        append_fp8_kernel<false><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
     if (a.num_tokens <= 0) return cudaSuccess;

@@ -51,9 +51,9 @@ using dec::Geo;
 using dec::kHeadsPerCta;
 using dec::kMaxTable;
 
-template <int D, int CW, int STAGES>
+template <int D, int CW, int STAGES, int EB = 2>
 struct Smem {
-    using G = Geo<D, CW>;
+    using G = Geo<D, CW, EB>;
     static constexpr size_t kRing = 2 * STAGES * G::kStage;
     static constexpr size_t kArena = kRing > size_t(G::kScratch) ? kRing : size_t(G::kScratch);  // scratch aliases the ring
     static constexpr size_t kBars = kArena;
@@ -62,12 +62,25 @@ struct Smem {
     static constexpr size_t kBytes = kMisc + 16;
 };
 
-template <typename T, int D, int CW, int STAGES, bool MQ>
+// A query pair (two elements of T) as the f16 pair the E4M3 path multiplies with.
+template <typename T>
+__device__ __forceinline__ uint32_t q_as_f16x2(uint32_t x);
+template <>
+__device__ __forceinline__ uint32_t q_as_f16x2<__half>(uint32_t x) { return x; }
+template <>
+__device__ __forceinline__ uint32_t q_as_f16x2<__nv_bfloat16>(uint32_t x) {
+    return Mma<__half>::pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+
+// KV8: the pools hold E4M3 codes (head_dim 128); the tensor cores run in f16.
+template <typename T, int D, int CW, int STAGES, bool MQ, bool KV8 = false>
 __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                      const __grid_constant__ CUtensorMap tmv,
                                                                      const DecodeArgs a) {
-    using G = Geo<D, CW>;
-    using S = Smem<D, CW, STAGES>;
+    static_assert(!KV8 || (D == 128 && !MQ), "E4M3 pools: head_dim 128, one query token");
+    constexpr int kEB = KV8 ? 1 : 2;                // bytes of a pool element
+    using G = Geo<D, CW, kEB>;
+    using S = Smem<D, CW, STAGES, kEB>;
     constexpr int kChunk = G::kChunk;
     constexpr int kConsumers = G::kConsumers;
     constexpr int kThreads = G::kThreads;
@@ -127,6 +140,18 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         for (int k = 0; k < kTePerLane; ++k) {
             const int i = lane + 32 * k;
             te[k] = (32 * k < tcount && i < tcount) ? __ldg(row + i) : 0;
+        }
+    } else if constexpr (KV8) {
+        // Q^T in consume_chunk_fp8's order: lane holds q[n = lane/4][32*t + 4*ks + {0,1}]
+        // and [.. + {2,3}] (t = lane % 4), as f16 (exact for |q| < 65504)
+        const int n = lane >> 2;
+        const int nq = min(n, gc - 1);
+        const T* qrow = reinterpret_cast<const T*>(a.q) + dec::qo_row<MQ>(a, sh0, s, kvh, vh0, nq) * D + 32 * (lane & 3);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qrow + 4 * ks));
+            ws.qb[ks][0] = n < gc ? q_as_f16x2<T>(raw.x) : 0u;
+            ws.qb[ks][1] = n < gc ? q_as_f16x2<T>(raw.y) : 0u;
         }
     } else {
         // Q^T as the B operand (k = head_dim, n = query head): lane holds
@@ -206,7 +231,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
                 }
                 const int tok0 = start + c * kChunk;
                 const int nb = (min(end, tok0 + kChunk) - tok0 + bs - 1) / bs;
-                mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * 2 * 2));
+                mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * kEB * 2));
                 for (int j = 0; j < nb; ++j) {
                     const int pb = tbl[c * per_chunk + j];
 #pragma unroll
@@ -223,6 +248,9 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
 
     // ================================================================ consumer warps
     dec::reset_state(ws);
+    // an E4M3 pool's K scale multiplies every score of this KV head
+    float sl2 = a.scale_log2;
+    if constexpr (KV8) sl2 *= __ldg(a.k_scale + kvh);
     // causal limits of this lane's two query-row columns (all L for decode)
     const int lim0 = vh0 + 2 * (lane & 3) < a.group ? dec::causal_limit<MQ>(a, L, vh0 + 2 * (lane & 3)) : L;
     const int lim1 = vh0 + 2 * (lane & 3) + 1 < a.group ? dec::causal_limit<MQ>(a, L, vh0 + 2 * (lane & 3) + 1) : L;
@@ -247,9 +275,15 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         }
         const int tokw = start + c * kChunk + warp * 16;
         const int nv = min(16, end - tokw);
-        if (nv > 0)
-            dec::consume_chunk<T, D, CW, MQ>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage), nv,
-                                         warp, lane, a.scale_log2, tokw, lim0, lim1);
+        if (nv > 0) {
+            if constexpr (KV8)
+                dec::consume_chunk_fp8<CW>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage), nv,
+                                           warp, lane, sl2);
+            else
+                dec::consume_chunk<T, D, CW, MQ>(ws, smem_u32(kring + st * G::kStage),
+                                                 smem_u32(vring + st * G::kStage), nv, warp, lane, a.scale_log2, tokw,
+                                                 lim0, lim1);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -266,7 +300,10 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     // chunk was consumed by every warp, so no copy is still landing)
     float* scratch = reinterpret_cast<float*>(kring);
     if (!epi_sync()) return;                      // every warp is done reading the ring
-    dec::warp_state_to_smem<D, CW>(ws, scratch, warp, lane);
+    if constexpr (KV8)
+        dec::warp_state_to_smem_fp8<CW>(ws, scratch, warp, lane, __ldg(a.v_scale + kvh));
+    else
+        dec::warp_state_to_smem<D, CW>(ws, scratch, warp, lane);
     if (!epi_sync()) return;
     dec::combine_warps<T, D, CW, MQ>(a, scratch, sh0, s, kvh, vh0, gc, part, nparts, threadIdx.x);
     if (nparts == 1) return;
@@ -285,11 +322,11 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     dec::merge_partitions<T, D, CW, MQ>(a, scratch, sh0, s, kvh, vh0, gc, nparts, warp, lane, threadIdx.x, epi_sync);
 }
 
-template <typename T, int D, int CW, int STAGES, bool MQ = false>
+template <typename T, int D, int CW, int STAGES, bool MQ = false, bool KV8 = false>
 cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
-    constexpr size_t smem = Smem<D, CW, STAGES>::kBytes;
+    constexpr size_t smem = Smem<D, CW, STAGES, KV8 ? 1 : 2>::kBytes;
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = decode_kernel<T, D, CW, STAGES, MQ>;
+    auto kern = decode_kernel<T, D, CW, STAGES, MQ, KV8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
@@ -307,10 +344,22 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensor
     return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
 }
 
+int fp8_stages();
+
 template <typename T, int D>
 cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int warps, int stages,
                        cudaStream_t s) {
     if (a.num_queries > 1) return launch_t<T, D, 4, 2, true>(a, tmk, tmv, s);   // verify: one shape
+    if (a.kv8) {                                    // E4M3 pools: stages of 64 positions (8 KB each of K, V)
+        if constexpr (D == 128) {
+            switch (fp8_stages()) {
+                case 2: return launch_t<T, D, 4, 2, false, true>(a, tmk, tmv, s);
+                case 3: return launch_t<T, D, 4, 3, false, true>(a, tmk, tmv, s);
+                default: return launch_t<T, D, 4, 4, false, true>(a, tmk, tmv, s);
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
     if (warps == 2) {
         switch (stages) {
             case 2: return launch_t<T, D, 2, 2>(a, tmk, tmv, s);
@@ -359,10 +408,10 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_
 }
 
 namespace {
-template <typename T, int D, int CW, int STAGES>
+template <typename T, int D, int CW, int STAGES, bool KV8 = false>
 int occupancy_of() {
-    constexpr size_t smem = Smem<D, CW, STAGES>::kBytes;
-    auto kern = decode_kernel<T, D, CW, STAGES, false>;
+    constexpr size_t smem = Smem<D, CW, STAGES, KV8 ? 1 : 2>::kBytes;
+    auto kern = decode_kernel<T, D, CW, STAGES, false, KV8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return 0;
     int n = 0;
@@ -377,13 +426,26 @@ int occupancy_cfg(int cw, int st) {
     return st == 3 ? occupancy_of<__half, D, 4, 3>() : st == 4 ? occupancy_of<__half, D, 4, 4>()
                                                                : occupancy_of<__half, D, 4, 2>();
 }
+
+// E4M3 pools: 4 stages unless PKV_DECODE_STAGES says otherwise
+int fp8_stages() {
+    static const int v = env_choice("PKV_DECODE_STAGES", 4, 2, 4);
+    return v;
+}
+
+int occupancy_fp8() {
+    const int st = fp8_stages();
+    return st == 2 ? occupancy_of<__half, 128, 4, 2, true>() : st == 3 ? occupancy_of<__half, 128, 4, 3, true>()
+                                                                       : occupancy_of<__half, 128, 4, 4, true>();
+}
 }  // namespace
 
-int decode_ctas_per_sm(int head_dim) {
-    static int cache[2] = {-1, -1};               // per head_dim; the same on every GB300
-    const int i = head_dim == 64 ? 0 : 1;
-    if (cache[i] < 0) cache[i] = i == 0 ? occupancy_cfg<64>(consumer_warps(), ring_stages())
-                                        : occupancy_cfg<128>(consumer_warps(), ring_stages());
+int decode_ctas_per_sm(int head_dim, bool kv8) {
+    static int cache[3] = {-1, -1, -1};           // head_dim 64, 128, E4M3; the same on every GB300
+    const int i = kv8 ? 2 : head_dim == 64 ? 0 : 1;
+    if (cache[i] < 0) cache[i] = kv8 ? occupancy_fp8()
+                                     : i == 0 ? occupancy_cfg<64>(consumer_warps(), ring_stages())
+                                              : occupancy_cfg<128>(consumer_warps(), ring_stages());
     return cache[i];
 }
 

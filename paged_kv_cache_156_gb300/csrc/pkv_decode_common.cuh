@@ -3,6 +3,7 @@
 // partitions; MQ instantiates the multi-query (verify) form.
 #pragma once
 
+#include <cuda_fp8.h>
 #include <float.h>
 
 #include "pkv_device.cuh"
@@ -15,13 +16,14 @@ constexpr int kMaxTable = 512;       // staged table entries: part_tokens (<= 40
 constexpr int kHeadsPerCta = 8;      // mma N: query heads served by one CTA
 constexpr int kMaxParts = 512;       // partitions per sequence the in-kernel merge handles
 
-// CW consumer warps each own 16 positions of a chunk of 16 * CW positions.
-template <int D, int CW>
+// CW consumer warps each own 16 positions of a chunk of 16 * CW positions;
+// EB is the pool's element size (2: fp16 / bf16; 1: E4M3 codes).
+template <int D, int CW, int EB = 2>
 struct Geo {
     static constexpr int kChunk = 16 * CW;              // positions per pipeline stage
     static constexpr int kConsumers = 32 * CW;
     static constexpr int kThreads = kConsumers + 32;    // plus one producer warp
-    static constexpr int kHalves = D / 64;              // 64-element (128-byte) column planes
+    static constexpr int kHalves = D * EB / 128;        // 128-byte column planes
     static constexpr int kPlane = kChunk * 128;         // bytes of one plane of a chunk
     static constexpr int kStage = kHalves * kPlane;     // bytes of K (or V) of one chunk
     static constexpr int kScratch = (CW * kHeadsPerCta * (D + 2) + 2 * kHeadsPerCta) * 4;  // merge scratch
@@ -184,6 +186,141 @@ __device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uin
         uint32_t vf[4];
         ldmatrix_x4_trans(vf, swz(vst + (mt >> 2) * G::kPlane, vrow, (mt & 3) * 2 + vcol));
         M::run(w.o[mt], vf, pb0, pb1);
+    }
+}
+
+// ---------------------------------------------------------------- 8-bit (E4M3) pools
+// Four E4M3 codes (a 32-bit word, byte 0 first) to two f16 pairs: lo =
+// (byte 0, byte 1), hi = (byte 2, byte 3), the first of each in the low half.
+// Every E4M3 value is exact in f16.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// One warp's 16 positions of a chunk of an E4M3 pool (head_dim 128, one
+// 128-byte swizzled plane per stage).  The tensor cores run in f16: each
+// lane reads its K and V bytes from shared memory and converts them in
+// registers.  The contraction index of S^T = K Q^T is permuted so that a
+// lane's K bytes are contiguous: logical k = 16*ks + 2*t + j (t = lane % 4,
+// j in {0, 1, 8, 9}) is head-dim element 32*t + 4*ks + {0, 1, 2, 3}[j]; Q is
+// loaded in the same order, so the dot products are unchanged.  For O^T =
+// V^T P^T the rows of tile mt are head-dim elements 16*g + 2*mt (row g) and
+// 16*g + 2*mt + 1 (row g + 8), g = lane / 4, so a lane reads 16 contiguous
+// bytes of each of its four positions; warp_state_to_smem_fp8 undoes it.
+template <int CW>
+__device__ __forceinline__ void consume_chunk_fp8(WarpState<128>& w, uint32_t kst, uint32_t vst, int nv, int warp,
+                                                  int lane, float sl2) {
+    using M = Mma<__half>;
+    const int g = lane >> 2, t = lane & 3;
+    const int row0 = warp * 16 + g;
+    // ---- S^T = K Q^T: this lane's 32 bytes of K rows g and g + 8
+    const uint4 ka0 = ld_shared_v4(swz(kst, row0, 2 * t)), ka1 = ld_shared_v4(swz(kst, row0, 2 * t + 1));
+    const uint4 kb0 = ld_shared_v4(swz(kst, row0 + 8, 2 * t)), kb1 = ld_shared_v4(swz(kst, row0 + 8, 2 * t + 1));
+    const uint32_t kra[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+    const uint32_t krb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+    float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t af[4];                            // rows g, g+8 at logical k (2t, 2t+1), then (2t+8, 2t+9)
+        e4m3x4_to_f16x2x2(kra[ks], af[0], af[2]);
+        e4m3x4_to_f16x2x2(krb[ks], af[1], af[3]);
+        M::run(sacc, af, w.qb[ks][0], w.qb[ks][1]);
+    }
+    // ---- online softmax, as consume_chunk (one query token per sequence)
+    const bool va = g < nv, vb = g + 8 < nv;
+    const float s0 = va ? sacc[0] * sl2 : -INFINITY;
+    const float s1 = va ? sacc[1] * sl2 : -INFINITY;
+    const float s2 = vb ? sacc[2] * sl2 : -INFINITY;
+    const float s3 = vb ? sacc[3] * sl2 : -INFINITY;
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(w.m0, mx0), mn1 = fmaxf(w.m1, mx1);
+    const float al0 = fast_exp2(w.m0 - mn0), al1 = fast_exp2(w.m1 - mn1);
+    w.m0 = mn0;
+    w.m1 = mn1;
+    const uint32_t p01 = M::pack(fast_exp2(s0 - mn0), fast_exp2(s1 - mn1));
+    const uint32_t p23 = M::pack(fast_exp2(s2 - mn0), fast_exp2(s3 - mn1));
+    const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);
+    w.l0 = w.l0 * al0 + f01.x + f23.x;
+    w.l1 = w.l1 * al1 + f01.y + f23.y;
+    // the accumulators need rescaling only when some column's maximum moved
+    if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            w.o[mt][0] *= al0;
+            w.o[mt][1] *= al1;
+            w.o[mt][2] *= al0;
+            w.o[mt][3] *= al1;
+        }
+    }
+    // ---- O^T += V^T P^T: bytes 16g .. 16g+15 of positions 2t, 2t+1, 2t+8, 2t+9;
+    // positions past seq_len may hold NaN codes and are zeroed
+    const uint32_t pb0 = movmatrix_trans(p01);
+    const uint32_t pb1 = movmatrix_trans(p23);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 v0 = 2 * t < nv ? ld_shared_v4(swz(vst, warp * 16 + 2 * t, g)) : z;
+    const uint4 v1 = 2 * t + 1 < nv ? ld_shared_v4(swz(vst, warp * 16 + 2 * t + 1, g)) : z;
+    const uint4 v2 = 2 * t + 8 < nv ? ld_shared_v4(swz(vst, warp * 16 + 2 * t + 8, g)) : z;
+    const uint4 v3 = 2 * t + 9 < nv ? ld_shared_v4(swz(vst, warp * 16 + 2 * t + 9, g)) : z;
+    const uint32_t V0[4] = {v0.x, v0.y, v0.z, v0.w}, V1[4] = {v1.x, v1.y, v1.z, v1.w};
+    const uint32_t V2[4] = {v2.x, v2.y, v2.z, v2.w}, V3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int r = mt >> 1, b = (mt & 1) * 2;           // bytes 2mt, 2mt + 1 of the 16
+        const unsigned sel = b | ((4 + b) << 4) | ((b + 1) << 8) | ((5 + b) << 12);
+        const uint32_t x01 = __byte_perm(V0[r], V1[r], sel);   // (pos 2t, 2t+1) at d, then at d + 1
+        const uint32_t x89 = __byte_perm(V2[r], V3[r], sel);   // (pos 2t+8, 2t+9)
+        uint32_t vf[4];
+        e4m3x4_to_f16x2x2(x01, vf[0], vf[1]);
+        e4m3x4_to_f16x2x2(x89, vf[2], vf[3]);
+        M::run(w.o[mt], vf, pb0, pb1);
+    }
+}
+
+// As warp_state_to_smem for the E4M3 path: undoes the head-dim permutation of
+// consume_chunk_fp8 and applies the V scale to the partial output.
+template <int CW>
+__device__ __forceinline__ void warp_state_to_smem_fp8(const WarpState<128>& w, float* scratch, int warp, int lane,
+                                                       float vscale) {
+    float l0 = w.l0, l1 = w.l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float* sm_m = scratch;
+    float* sm_l = sm_m + CW * kHeadsPerCta;
+    float* sm_o = sm_l + CW * kHeadsPerCta;
+    if (lane < 4) {
+        sm_m[warp * kHeadsPerCta + 2 * lane] = w.m0;
+        sm_m[warp * kHeadsPerCta + 2 * lane + 1] = w.m1;
+        sm_l[warp * kHeadsPerCta + 2 * lane] = l0;
+        sm_l[warp * kHeadsPerCta + 2 * lane + 1] = l1;
+    }
+    const int hA = 2 * (lane & 3);
+    float* oa = sm_o + (warp * kHeadsPerCta + hA) * 128;
+    float* ob = oa + 128;
+    const int g = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = 16 * g + 2 * mt;
+        oa[d0] = w.o[mt][0] * vscale;
+        ob[d0] = w.o[mt][1] * vscale;
+        oa[d0 + 1] = w.o[mt][2] * vscale;
+        ob[d0 + 1] = w.o[mt][3] * vscale;
     }
 }
 

@@ -11,7 +11,8 @@
 //
 //  * partition size: at least the host's choice; when the call asks for the
 //    automatic size, about 0.85 x the positions per resident CTA slot
-//    (sum_s L_s * KV head groups / slots), in multiples of 512, capped by the
+//    (sum_s L_s * KV head groups / slots; twice that for an E4M3 pool, whose
+//    positions are half the bytes), in multiples of 512, capped by the
 //    longest sequence and by the staged table, and raised when the item count
 //    would spill a quarter wave or less past one full wave;
 //  * order: groups of adjacent sequences that share their first physical
@@ -127,7 +128,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
         const long long W = block_sum(L, next());
         const int lmax = block_max(L, next());
         const long long slots = a.slots > 0 ? a.slots : 1;
-        const long long target = (W * nh * 17) / (slots * 20);              // 0.85 x positions per slot
+        // 0.85 x the positions per slot, counted in 16-bit-pool bytes: an E4M3
+        // position is half the bytes, so its partitions are twice as long
+        const long long target = (W * nh * (a.kv8 ? 34 : 17)) / (slots * 20);
         long long p = ((target + kGranule / 2) / kGranule) * kGranule;       // nearest multiple of 512
         p = max(p, static_cast<long long>(kGranule));
         const int table_cap = dec::kMaxTable * a.block_size;

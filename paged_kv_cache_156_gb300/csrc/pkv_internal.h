@@ -22,6 +22,25 @@ struct AppendArgs {
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 
+// Append into an E4M3 pool: each element is quantized as
+// e4m3(float32(x) / float32(scale[head])), round to nearest even, saturating.
+struct AppendFp8Args {
+    const uint4* k;          // [T][row_vecs] 8 fp16 / bf16 elements per vector
+    const uint4* v;
+    uint2* key_cache;        // [num_blocks * block_size][row_vecs] 8 codes per vector
+    uint2* value_cache;
+    const int64_t* slots;
+    const float* k_scale;    // [num_kv_heads]
+    const float* v_scale;
+    int64_t num_tokens;
+    int64_t num_slots;
+    int row_vecs;            // num_kv_heads * head_dim / 8
+    int head_vecs;           // head_dim / 8
+    int bf16;                // input elements: 0 = fp16, 1 = bf16
+    unsigned* err;
+};
+cudaError_t launch_append_fp8(const AppendFp8Args& a, cudaStream_t s);
+
 // Block copies between two pools of the same block shape (the same pool for
 // copy-on-write, a device pool and a pinned host pool for swapping).
 struct CopyArgs {
@@ -68,6 +87,9 @@ struct DecodeArgs {
     int max_parts;                   // ceil(max_seq_len / part_tokens): the partials' stride
     int plan_capacity;               // num_seqs * max_parts: entries of `plan` (the grid's work slots)
     float scale_log2;                // scale * log2(e)
+    int kv8;                         // 1: the pools hold E4M3 codes (head_dim 128), scaled per KV head
+    const float* k_scale;            // [num_kv_heads] (E4M3 pools only)
+    const float* v_scale;
 };
 
 // Sequences a call plans (sorts and compacts) at most; larger batches run the
@@ -94,8 +116,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
 cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s);
 
 // CTAs of the decode kernel resident per SM on the current device (current
-// configuration), or 0 if it cannot be queried.
-int decode_ctas_per_sm(int head_dim);
+// configuration; kv8: the E4M3-pool kernel), or 0 if it cannot be queried.
+int decode_ctas_per_sm(int head_dim, bool kv8 = false);
 
 // Record `msg` as the calling thread's pkv_last_error() message and return `st`.
 int set_error_message(int st, const char* msg);
