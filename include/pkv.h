@@ -177,6 +177,48 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, const vo
                                       void* stream);
 
 /*
+ * Plan once, run per layer.  Every layer of a decode step attends over the
+ * same batch (the same lengths and block tables), so the work list the plan
+ * kernel builds (above) is the same for all of them.  pkv_decode_plan writes
+ * it into `workspace` (and zeroes the merge tickets) on `stream`;
+ * pkv_paged_attention_decode_planned and pkv_paged_attention_decode_fp8_planned
+ * then run the decode alone, each exactly as pkv_paged_attention_decode /
+ * _fp8 would, leaving the tickets zeroed again for the next run.
+ *
+ * Preconditions (not checked on the host): the runs pass the same
+ * block_tables contents, seq_lens contents, num_seqs, max_seq_len, num_heads,
+ * num_kv_heads, head_dim, block_size and partition_tokens as the plan; kv_dt
+ * is the pools' element type (PKV_E4M3 for the _fp8 runs); calls are ordered
+ * on one stream; the plan is made again after any call that raised the
+ * device error word.  A run whose work list does not fit its arguments skips
+ * the offending entries and raises the error word's bounds bit; it never
+ * reads or writes outside its buffers.  A batch above PKV_PLAN_MAX_SEQS has
+ * no work list: pkv_decode_plan does nothing and each run launches its full
+ * grid.
+ */
+PKV_API pkv_status pkv_decode_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                           int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                           int block_size, pkv_dtype kv_dt, void* workspace, size_t workspace_bytes,
+                           int partition_tokens, void* stream);
+
+PKV_API pkv_status pkv_paged_attention_decode_planned(void* out, const void* q, const void* key_cache,
+                                              const void* value_cache, const int32_t* block_tables,
+                                              int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                              int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                              int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                              void* workspace, size_t workspace_bytes, int partition_tokens,
+                                              void* stream);
+
+PKV_API pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void* q, const void* key_cache,
+                                                  const void* value_cache, const int32_t* block_tables,
+                                                  int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                                  int max_seq_len, int num_heads, int num_kv_heads,
+                                                  int head_dim, int block_size, int64_t num_blocks, float scale,
+                                                  pkv_dtype dt, const float* k_scale, const float* v_scale,
+                                                  void* workspace, size_t workspace_bytes, int partition_tokens,
+                                                  void* stream);
+
+/*
  * paged_attention_verify -- num_queries query tokens per sequence over its
  * paged K/V, causal among themselves (the verification step of speculative
  * decoding).

@@ -31,7 +31,8 @@ ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_deco
                "pkv_paged_attention_decode_static", "pkv_swap_blocks", "pkv_paged_attention_verify", "pkv_bm_create", "pkv_bm_destroy",
                "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
                "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables", "pkv_paged_kv_append_fp8",
-               "pkv_paged_attention_decode_fp8")
+               "pkv_paged_attention_decode_fp8", "pkv_decode_plan", "pkv_paged_attention_decode_planned",
+               "pkv_paged_attention_decode_fp8_planned")
 
 _lib = None
 
@@ -74,6 +75,12 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode_fp8.restype = c_i
     lib.pkv_paged_attention_decode_fp8.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                    c_i64, c_f, c_i, c_p, c_p, c_p, c_sz, c_i, c_p]
+    lib.pkv_paged_attention_decode_fp8_planned.restype = c_i
+    lib.pkv_paged_attention_decode_fp8_planned.argtypes = lib.pkv_paged_attention_decode_fp8.argtypes
+    lib.pkv_paged_attention_decode_planned.restype = c_i
+    lib.pkv_paged_attention_decode_planned.argtypes = lib.pkv_paged_attention_decode.argtypes
+    lib.pkv_decode_plan.restype = c_i
+    lib.pkv_decode_plan.argtypes = [c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_copy_blocks.restype = c_i
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p, c_i64, c_i64, c_i, c_i,
                                     c_i, c_i, c_p]
@@ -166,14 +173,31 @@ def alloc_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, pa
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def decode_plan(workspace, block_tables, seq_lens, num_heads, key_cache, max_seq_len, partition_tokens=0) -> None:
+    """The work list of a decode batch, once per step (``pkv_decode_plan``): the runs that pass
+    ``planned=True`` over the same batch then skip the plan kernel.  ``key_cache`` gives the pool's
+    shape and element type (uint8: E4M3)."""
+    NB, bs, Hkv, d = _pool("key_cache", key_cache, tuple(_POOL_DT))
+    B = seq_lens.shape[0]
+    _cuda("block_tables", block_tables, torch.int32, 2)
+    _cuda("seq_lens", seq_lens, torch.int32, 1)
+    _check(load().pkv_decode_plan(ctypes.c_void_p(block_tables.data_ptr()), block_tables.shape[1],
+                                  ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), num_heads, Hkv, d, bs,
+                                  _POOL_DT[key_cache.dtype], _cuda("workspace", workspace),
+                                  workspace.numel() * workspace.element_size(), int(partition_tokens),
+                                  _stream(workspace)))
+
+
 def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, block_size=None,
-                           num_kv_heads=None, max_seq_len=None, workspace=None, partition_tokens=0) -> None:
+                           num_kv_heads=None, max_seq_len=None, workspace=None, partition_tokens=0,
+                           planned=False) -> None:
     """out[s, h] = softmax(scale * q[s, h] . K) V over positions [0, seq_lens[s]) of KV head h // G.
 
     q, out: [B, Hq, d]; caches [NB, bs, Hkv, d]; block_tables int32 [B, W]; seq_lens int32 [B].
     ``max_seq_len`` is the host-known bound of seq_lens (read from the device
     if omitted, which synchronises).  ``workspace``: see ``alloc_workspace``
-    (allocated here when omitted).
+    (allocated here when omitted).  ``planned``: run over the work list
+    ``decode_plan`` put in ``workspace`` for this batch (no plan kernel).
     """
     NB, bs, Hkv, d = _pool("key_cache", key_cache)
     if block_size is not None and block_size != bs:
@@ -198,9 +222,9 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_len
         workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
     ws_ptr = _cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().pkv_paged_attention_decode(
-        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
-        NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
+    fn = load().pkv_paged_attention_decode_planned if planned else load().pkv_paged_attention_decode
+    _check(fn(*ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
+              NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
 
 
 def _scales(name, t, Hkv):
@@ -228,7 +252,7 @@ def paged_kv_append_fp8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_s
 
 
 def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq_lens, k_scale, v_scale, scale=None,
-                               max_seq_len=None, workspace=None, partition_tokens=0) -> None:
+                               max_seq_len=None, workspace=None, partition_tokens=0, planned=False) -> None:
     """paged_attention_decode over uint8 E4M3 pools: K = e4m3(code) * k_scale[g], V = e4m3(code) * v_scale[g];
     q, out fp16 / bf16 [B, Hq, 128]; k_scale, v_scale float32 [Hkv]."""
     NB, bs, Hkv, d = _pool("key_cache", key_cache, (torch.uint8,))
@@ -250,7 +274,8 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq
         workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
     ws_ptr = _cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().pkv_paged_attention_decode_fp8(
+    fn = load().pkv_paged_attention_decode_fp8_planned if planned else load().pkv_paged_attention_decode_fp8
+    _check(fn(
         *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
         NB, float(scale), _DT[q.dtype], _scales("k_scale", k_scale, Hkv), _scales("v_scale", v_scale, Hkv), ws_ptr,
         ws_bytes, int(partition_tokens), _stream(q)))

@@ -247,16 +247,20 @@ int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, i
 namespace {
 
 // Decode (num_queries == 1) and multi-query verify share one path: a KV head
-// serves (num_heads / num_kv_heads) * num_queries query rows.
+// serves (num_heads / num_kv_heads) * num_queries query rows.  `mode`: plan
+// and run (one call), plan only (pkv_decode_plan; q, out and the pools are
+// not used), or run only over the plan already in the workspace.
 pkv_status attention_call(void* out, const void* q, const void* key_cache, const void* value_cache,
                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
                           int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
                           int64_t num_blocks, float scale, pkv_dtype dt, int num_queries, void* workspace,
                           size_t workspace_bytes, int partition_tokens, void* stream, const float* k_scale = nullptr,
-                          const float* v_scale = nullptr) {
+                          const float* v_scale = nullptr, pkv::DecodeMode mode = pkv::DecodeMode::kPlanAndRun,
+                          bool kv8_plan = false) {
+    const bool runs = mode != pkv::DecodeMode::kPlanOnly;
     pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
     if (st != PKV_OK) return st;
-    const bool kv8 = k_scale || v_scale;                  // an E4M3 pool (the _fp8 entry point)
+    const bool kv8 = runs ? (k_scale || v_scale) : kv8_plan;    // an E4M3 pool (the _fp8 entry points)
     if (kv8 && (head_dim != 128 || num_queries != 1))
         return fail(PKV_ERR_UNSUPPORTED, "E4M3 pools: head_dim 128 and one query token only");
     if (num_queries < 1 || num_queries > 64) return fail(PKV_ERR_INVALID, "num_queries %d outside [1, 64]", num_queries);
@@ -268,17 +272,21 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     if (max_blocks_per_seq < 0 || static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
         return fail(PKV_ERR_INVALID, "max_seq_len %d exceeds max_blocks_per_seq %d * block_size %d", max_seq_len,
                     max_blocks_per_seq, block_size);
-    if (!isfinite(scale)) return fail(PKV_ERR_INVALID, "scale is not finite");
+    if (runs && !isfinite(scale)) return fail(PKV_ERR_INVALID, "scale is not finite");
     if (partition_tokens < 0 || partition_tokens > kMaxPartition || partition_tokens % kChunk != 0)
         return fail(PKV_ERR_INVALID, "partition_tokens %d: 0 or a multiple of 64 up to 4096", partition_tokens);
     if (num_seqs == 0) return ok();
-    if (!out || !q || !key_cache || !value_cache || !block_tables || !seq_lens || (kv8 && (!k_scale || !v_scale)))
-        return fail(PKV_ERR_INVALID, "null pointer");
-    if (kv8 && ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u)))
-        return fail(PKV_ERR_INVALID, "k_scale / v_scale must be 4-byte aligned");
-    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
-        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-        return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned; tables and lengths 4-byte");
+    if (!block_tables || !seq_lens) return fail(PKV_ERR_INVALID, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(PKV_ERR_INVALID, "tables and lengths must be 4-byte aligned");
+    if (runs) {
+        if (!out || !q || !key_cache || !value_cache || (kv8 && (!k_scale || !v_scale)))
+            return fail(PKV_ERR_INVALID, "null pointer");
+        if (kv8 && ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u)))
+            return fail(PKV_ERR_INVALID, "k_scale / v_scale must be 4-byte aligned");
+        if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+            return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned");
+    }
 
     const int dev = current_device();
     const int part = resolve_partition(num_seqs, rows, num_kv_heads, max_seq_len, partition_tokens, head_dim);
@@ -296,10 +304,13 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     if (static_cast<int64_t>(num_kv_heads) * ((group + 7) / 8) * max_parts * num_seqs >= (int64_t(1) << 31))
         return fail(PKV_ERR_UNSUPPORTED, "too many work items");
 
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk{}, tmv{};
     const int eb = kv8 ? 1 : 2;
-    if ((st = encode_pool(&tmk, key_cache, num_blocks, block_size, num_kv_heads, head_dim, eb)) != PKV_OK) return st;
-    if ((st = encode_pool(&tmv, value_cache, num_blocks, block_size, num_kv_heads, head_dim, eb)) != PKV_OK) return st;
+    if (runs) {
+        if ((st = encode_pool(&tmk, key_cache, num_blocks, block_size, num_kv_heads, head_dim, eb)) != PKV_OK) return st;
+        if ((st = encode_pool(&tmv, value_cache, num_blocks, block_size, num_kv_heads, head_dim, eb)) != PKV_OK)
+            return st;
+    }
 
     pkv::DecodeArgs a;
     a.out = out;
@@ -333,7 +344,8 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.kv8 = kv8;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
-    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream));
+    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream),
+                                       mode);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -360,6 +372,44 @@ pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt,
                           num_queries, workspace, workspace_bytes, partition_tokens, stream);
+}
+
+pkv_status pkv_decode_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                           int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           pkv_dtype kv_dt, void* workspace, size_t workspace_bytes, int partition_tokens,
+                           void* stream) {
+    if (!valid_dtype(kv_dt) && kv_dt != PKV_E4M3) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(kv_dt));
+    return attention_call(nullptr, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, 1, 1.0f,
+                          kv_dt == PKV_E4M3 ? PKV_F16 : kv_dt, 1, workspace, workspace_bytes, partition_tokens,
+                          stream, nullptr, nullptr, pkv::DecodeMode::kPlanOnly, kv_dt == PKV_E4M3);
+}
+
+pkv_status pkv_paged_attention_decode_planned(void* out, const void* q, const void* key_cache,
+                                              const void* value_cache, const int32_t* block_tables,
+                                              int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                              int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                              int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                              void* workspace, size_t workspace_bytes, int partition_tokens,
+                                              void* stream) {
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
+                          workspace, workspace_bytes, partition_tokens, stream, nullptr, nullptr,
+                          pkv::DecodeMode::kRunOnly);
+}
+
+pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void* q, const void* key_cache,
+                                                  const void* value_cache, const int32_t* block_tables,
+                                                  int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                                  int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                                  const float* k_scale, const float* v_scale, void* workspace,
+                                                  size_t workspace_bytes, int partition_tokens, void* stream) {
+    if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "k_scale / v_scale are required");
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
+                          workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale,
+                          pkv::DecodeMode::kRunOnly);
 }
 
 pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,

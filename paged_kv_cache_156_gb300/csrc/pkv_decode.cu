@@ -110,6 +110,12 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         Lp = it.z;
         P = it.w;
         if (s < 0) return;                          // padding entry
+        // a plan made for other batch arguments (a run-only call's misuse): never index out of range
+        if (s >= a.num_seqs || part < 0 || Lp < 0 || Lp > a.max_seq_len || P < 64 || P > kMaxTable * a.block_size ||
+            part * P >= max(Lp, 1) || (Lp + P - 1) / P > a.max_parts) {
+            if (threadIdx.x == 0) raise_error(a.err, kErrBounds);
+            return;
+        }
     } else {
         hh = blockIdx.x;                            // KV head * head_groups + query-head group
         part = blockIdx.y;
@@ -312,9 +318,11 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     if (!epi_sync()) return;
     if (threadIdx.x == 0) {
         __threadfence();
-        const unsigned t = atomicAdd(a.tickets + static_cast<int64_t>(s) * a.num_kv_heads * a.head_groups + hh, 1u);
+        unsigned* ticket = a.tickets + static_cast<int64_t>(s) * a.num_kv_heads * a.head_groups + hh;
+        const unsigned t = atomicAdd(ticket, 1u);
         __threadfence();
         *merge_flag = (t == static_cast<unsigned>(nparts - 1));
+        if (t == static_cast<unsigned>(nparts - 1)) *ticket = 0u;   // every partition has taken it: reset for the next run
     }
     if (!epi_sync()) return;
     if (!*merge_flag) return;
@@ -450,11 +458,14 @@ int decode_ctas_per_sm(int head_dim, bool kv8) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, cudaStream_t s) {
+                          int head_dim, cudaStream_t s, DecodeMode mode) {
     if (a.num_seqs <= 0) return cudaSuccess;
     cudaError_t e = cudaSuccess;
     if (a.plan) {
-        e = launch_decode_plan(a, s);
+        if (mode != DecodeMode::kRunOnly) e = launch_decode_plan(a, s);
+        if (mode == DecodeMode::kPlanOnly) return e;
+    } else if (mode == DecodeMode::kPlanOnly) {
+        return cudaSuccess;                         // a full-grid batch plans nothing
     } else if (a.max_parts > 1) {
         const size_t n = sizeof(unsigned) * static_cast<size_t>(a.num_seqs) * a.num_kv_heads * a.head_groups;
         e = cudaMemsetAsync(a.tickets, 0, n, s);

@@ -108,11 +108,17 @@ struct DecodeWorkspace {
 };
 DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_parts);
 
+// What one decode call launches: the plan kernel then the decode kernel; the
+// plan alone; or the decode kernel alone over the plan already in the
+// workspace (the merging CTA zeroes its ticket, so a plan serves any number
+// of runs).
+enum class DecodeMode { kPlanAndRun, kPlanOnly, kRunOnly };
+
 // dtype: 0 = f16, 1 = bf16.  Runs one decode call on stream `s`: the plan
 // kernel (work list + tickets) or, for a batch above kPlanMaxSeqs, a ticket
 // memset; then the decode kernel, which merges split partitions in-kernel.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, cudaStream_t s);
+                          int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
 cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s);
 
 // CTAs of the decode kernel resident per SM on the current device (current
