@@ -13,8 +13,11 @@
 //    automatic size, about 0.85 x the positions per resident CTA slot
 //    (sum_s L_s * KV head groups / slots; twice that for an E4M3 pool, whose
 //    positions are half the bytes), in multiples of 512, capped by the
-//    longest sequence and by the staged table, and raised when the item count
-//    would spill a quarter wave or less past one full wave;
+//    longest sequence and by the staged table, raised when the item count
+//    would spill a quarter wave or less past one full wave, then shrunk to
+//    the smallest multiple of 64 that splits the longest sequence into as
+//    many partitions when that adds no work items (equal partitions on the
+//    critical path);
 //  * order: groups of adjacent sequences that share their first physical
 //    block (forks of one prompt, "LLM 推理引擎内部原理" §3.3) stay together, so
 //    their shared prefix is read while it is still in L2; groups are ordered
@@ -147,6 +150,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
                     break;
                 }
             }
+        }
+        // balance the longest sequence's partitions: the smallest multiple of 64 that still
+        // covers it in as many partitions, when that adds no work items (the critical path
+        // shortens; more items cost more than they save)
+        if (lmax > 0) {
+            const int parts = (lmax + P - 1) / P;
+            const int q = max(a.part_tokens, ((lmax + parts - 1) / parts + 63) / 64 * 64);
+            if (q < P && block_sum(t < B ? max(1, (L + q - 1) / q) : 0, next()) <=
+                             block_sum(t < B ? max(1, (L + P - 1) / P) : 0, next()))
+                P = q;
         }
     } else {
         __syncthreads();                            // sB0 complete
