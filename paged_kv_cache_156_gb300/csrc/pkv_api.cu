@@ -332,11 +332,15 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.qgroup = num_heads / num_kv_heads;
     a.num_queries = num_queries;
     a.group = a.qgroup * num_queries;
-    a.head_groups = (a.group + 7) / 8;
+    // more than kVerifyMinRows query rows per KV head: the verify kernel, 64 rows per CTA
+    const bool verify_kernel = num_queries > 1 && a.group > pkv::kVerifyMinRows;
+    a.head_groups = verify_kernel ? (a.group + pkv::kVerifyRowsPerCta - 1) / pkv::kVerifyRowsPerCta
+                                  : (a.group + 7) / 8;
     a.block_size = block_size;
     a.part_tokens = part;
     a.part_auto = partition_tokens == 0;
-    a.slots = sm_count_of(dev) * pkv::decode_ctas_per_sm(head_dim, kv8);
+    a.slots = sm_count_of(dev) * (verify_kernel ? pkv::verify_ctas_per_sm(head_dim)
+                                                : pkv::decode_ctas_per_sm(head_dim, kv8));
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
     a.plan_capacity = num_seqs * static_cast<int>(max_parts);
@@ -344,8 +348,10 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.kv8 = kv8;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
-    cudaError_t e = pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim, static_cast<cudaStream_t>(stream),
-                                       mode);
+    cudaError_t e = verify_kernel ? pkv::launch_verify(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
+                                                       static_cast<cudaStream_t>(stream), mode)
+                                  : pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
+                                                       static_cast<cudaStream_t>(stream), mode);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
     return ok();
 }

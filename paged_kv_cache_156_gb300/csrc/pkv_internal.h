@@ -121,6 +121,14 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
                           int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
 cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s);
 
+// The multi-query (verify) kernel for more than kVerifyMinRows query rows per
+// KV head: up to 64 rows per CTA (head_groups = ceil(rows / 64)).
+constexpr int kVerifyMinRows = 16;
+constexpr int kVerifyRowsPerCta = 64;
+cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                          int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
+int verify_ctas_per_sm(int head_dim);
+
 // CTAs of the decode kernel resident per SM on the current device (current
 // configuration; kv8: the E4M3-pool kernel), or 0 if it cannot be queried.
 int decode_ctas_per_sm(int head_dim, bool kv8 = false);

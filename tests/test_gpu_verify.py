@@ -2,8 +2,10 @@
 
 The last num_queries positions of each sequence are the query tokens' own K/V;
 query token i sees positions < L - num_queries + i + 1.  Cases cover query
-rows that fit one 8-row group and several, one and several partitions, query
-tokens that see nothing in a late partition, and every block size.
+rows that fit one 8-row group and several, more than 16 rows per KV head (the
+rows-as-M kernel, one and two 64-row groups, partly filled warps), one and
+several partitions, query tokens that see nothing in a late partition, an
+empty sequence, both head sizes and every block size.
 """
 import numpy as np
 import pytest
@@ -32,6 +34,12 @@ CASES = [
          lens=("fixed", (4, 1025, 700, 64, 65))),
     dict(num_heads=4, num_kv_heads=4, head_dim=64, block_size=32, dtype=W.F16, nq=3, lens=("fixed", (3, 17, 2000))),
     dict(num_heads=12, num_kv_heads=4, head_dim=128, block_size=16, dtype=W.BF16, nq=5, lens=("fixed", (130, 5, 513))),
+    # more than 16 rows per KV head: the rows-as-M verify kernel (64 rows per CTA)
+    dict(num_heads=32, num_kv_heads=8, head_dim=128, block_size=16, dtype=W.BF16, nq=5,
+         lens=("fixed", (5, 6, 64, 65, 1500, 3000))),
+    dict(num_heads=16, num_kv_heads=2, head_dim=128, block_size=32, dtype=W.F16, nq=8, lens=("fixed", (8, 900, 77))),
+    dict(num_heads=8, num_kv_heads=1, head_dim=64, block_size=8, dtype=W.BF16, nq=10, lens=("fixed", (10, 400, 1025))),
+    dict(num_heads=64, num_kv_heads=8, head_dim=128, block_size=16, dtype=W.F16, nq=3, lens=("fixed", (0, 3, 2049, 700))),
 ]
 
 
