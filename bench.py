@@ -291,6 +291,7 @@ def run_pkv(args, rank, world, local):
     launches_per_step = (1 if len(wl.copy_pairs) else 0) + (1 if planned else 0) + spec.num_layers * (
         2 + (0 if planned or max_parts_min == 1 else 1))
 
+    total_len = int(wl.seq_lens.sum())             # the scheduler knows it; it sizes the decode grid
     ev_pairs = []
 
     def step(i, timed):
@@ -303,7 +304,8 @@ def run_pkv(args, rank, world, local):
             else:
                 pkv.paged_kv_append(k_new, v_new, kcs[l], vcs[l], slots)
             if l == 0:
-                pkv.decode_plan(ws, tables, lens, spec.num_heads, kcs[0], wl.max_seq_len, args.partition_tokens)
+                pkv.decode_plan(ws, tables, lens, spec.num_heads, kcs[0], wl.max_seq_len, args.partition_tokens,
+                                sum_seq_lens=total_len)
             rec = timed and l == 0
             if rec:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -311,7 +313,7 @@ def run_pkv(args, rank, world, local):
             decode = (functools.partial(pkv.paged_attention_decode_fp8, k_scale=k_scales[l], v_scale=v_scales[l])
                       if spec.fp8 else pkv.paged_attention_decode)
             decode(outs[l], q, kcs[l], vcs[l], tables, lens, scale=wl.scale, max_seq_len=wl.max_seq_len,
-                   workspace=ws, partition_tokens=args.partition_tokens, planned=True)
+                   workspace=ws, partition_tokens=args.partition_tokens, planned=True, sum_seq_lens=total_len)
             if rec:
                 b.record()
                 ev_pairs.append((a, b))

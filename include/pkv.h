@@ -185,9 +185,19 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, const vo
  * then run the decode alone, each exactly as pkv_paged_attention_decode /
  * _fp8 would, leaving the tickets zeroed again for the next run.
  *
+ * sum_seq_lens: the sum of seq_lens when the caller knows it (a scheduler
+ * does), else 0.  It only sizes the decode grid: the work list then needs at
+ * most num_seqs + sum_seq_lens / P entries (P the smallest partition size)
+ * instead of num_seqs * ceil(max_seq_len / P), and a mixed-length batch
+ * launches far fewer CTAs that find no work.  The plan kernel checks it
+ * against the real sum; a wrong value raises the error word's bounds bit
+ * (entries past the grid are then dropped and their outputs are undefined,
+ * never out of range).
+ *
  * Preconditions (not checked on the host): the runs pass the same
- * block_tables contents, seq_lens contents, num_seqs, max_seq_len, num_heads,
- * num_kv_heads, head_dim, block_size and partition_tokens as the plan; kv_dt
+ * block_tables contents, seq_lens contents, num_seqs, max_seq_len,
+ * sum_seq_lens, num_heads, num_kv_heads, head_dim, block_size and
+ * partition_tokens as the plan; kv_dt
  * is the pools' element type (PKV_E4M3 for the _fp8 runs); calls are ordered
  * on one stream; the plan is made again after any call that raised the
  * device error word.  A run whose work list does not fit its arguments skips
@@ -197,26 +207,26 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, const vo
  * grid.
  */
 PKV_API pkv_status pkv_decode_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
-                           int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                           int block_size, pkv_dtype kv_dt, void* workspace, size_t workspace_bytes,
-                           int partition_tokens, void* stream);
+                           int num_seqs, int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, pkv_dtype kv_dt, void* workspace,
+                           size_t workspace_bytes, int partition_tokens, void* stream);
 
 PKV_API pkv_status pkv_paged_attention_decode_planned(void* out, const void* q, const void* key_cache,
                                               const void* value_cache, const int32_t* block_tables,
                                               int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
-                                              int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                                              int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
-                                              void* workspace, size_t workspace_bytes, int partition_tokens,
-                                              void* stream);
+                                              int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int64_t num_blocks, float scale, pkv_dtype dt, void* workspace,
+                                              size_t workspace_bytes, int partition_tokens, void* stream);
 
 PKV_API pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void* q, const void* key_cache,
                                                   const void* value_cache, const int32_t* block_tables,
                                                   int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
-                                                  int max_seq_len, int num_heads, int num_kv_heads,
-                                                  int head_dim, int block_size, int64_t num_blocks, float scale,
-                                                  pkv_dtype dt, const float* k_scale, const float* v_scale,
-                                                  void* workspace, size_t workspace_bytes, int partition_tokens,
-                                                  void* stream);
+                                                  int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                                  int num_kv_heads, int head_dim, int block_size,
+                                                  int64_t num_blocks, float scale, pkv_dtype dt,
+                                                  const float* k_scale, const float* v_scale, void* workspace,
+                                                  size_t workspace_bytes, int partition_tokens, void* stream);
 
 /*
  * paged_attention_verify -- num_queries query tokens per sequence over its

@@ -76,11 +76,14 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode_fp8.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                    c_i64, c_f, c_i, c_p, c_p, c_p, c_sz, c_i, c_p]
     lib.pkv_paged_attention_decode_fp8_planned.restype = c_i
-    lib.pkv_paged_attention_decode_fp8_planned.argtypes = lib.pkv_paged_attention_decode_fp8.argtypes
+    lib.pkv_paged_attention_decode_fp8_planned.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i,
+                                                           c_i, c_i, c_i, c_i64, c_f, c_i, c_p, c_p, c_p, c_sz, c_i,
+                                                           c_p]
     lib.pkv_paged_attention_decode_planned.restype = c_i
-    lib.pkv_paged_attention_decode_planned.argtypes = lib.pkv_paged_attention_decode.argtypes
+    lib.pkv_paged_attention_decode_planned.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i,
+                                                       c_i, c_i, c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_decode_plan.restype = c_i
-    lib.pkv_decode_plan.argtypes = [c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_decode_plan.argtypes = [c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i, c_i, c_i, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_copy_blocks.restype = c_i
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p, c_i64, c_i64, c_i, c_i,
                                     c_i, c_i, c_p]
@@ -173,16 +176,19 @@ def alloc_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, pa
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def decode_plan(workspace, block_tables, seq_lens, num_heads, key_cache, max_seq_len, partition_tokens=0) -> None:
+def decode_plan(workspace, block_tables, seq_lens, num_heads, key_cache, max_seq_len, partition_tokens=0,
+                sum_seq_lens=0) -> None:
     """The work list of a decode batch, once per step (``pkv_decode_plan``): the runs that pass
     ``planned=True`` over the same batch then skip the plan kernel.  ``key_cache`` gives the pool's
-    shape and element type (uint8: E4M3)."""
+    shape and element type (uint8: E4M3).  ``sum_seq_lens``: the lengths' sum if known (sizes the
+    grid tighter; the runs must pass the same value)."""
     NB, bs, Hkv, d = _pool("key_cache", key_cache, tuple(_POOL_DT))
     B = seq_lens.shape[0]
     _cuda("block_tables", block_tables, torch.int32, 2)
     _cuda("seq_lens", seq_lens, torch.int32, 1)
     _check(load().pkv_decode_plan(ctypes.c_void_p(block_tables.data_ptr()), block_tables.shape[1],
-                                  ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), num_heads, Hkv, d, bs,
+                                  ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), int(sum_seq_lens),
+                                  num_heads, Hkv, d, bs,
                                   _POOL_DT[key_cache.dtype], _cuda("workspace", workspace),
                                   workspace.numel() * workspace.element_size(), int(partition_tokens),
                                   _stream(workspace)))
@@ -190,7 +196,7 @@ def decode_plan(workspace, block_tables, seq_lens, num_heads, key_cache, max_seq
 
 def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, block_size=None,
                            num_kv_heads=None, max_seq_len=None, workspace=None, partition_tokens=0,
-                           planned=False) -> None:
+                           planned=False, sum_seq_lens=0) -> None:
     """out[s, h] = softmax(scale * q[s, h] . K) V over positions [0, seq_lens[s]) of KV head h // G.
 
     q, out: [B, Hq, d]; caches [NB, bs, Hkv, d]; block_tables int32 [B, W]; seq_lens int32 [B].
@@ -222,9 +228,15 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_len
         workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
     ws_ptr = _cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    fn = load().pkv_paged_attention_decode_planned if planned else load().pkv_paged_attention_decode
-    _check(fn(*ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
-              NB, float(scale), _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
+    lens_arg = [ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len)]
+    if planned:
+        _check(load().pkv_paged_attention_decode_planned(
+            *ptrs, block_tables.shape[1], *lens_arg, int(sum_seq_lens), Hq, Hkv, d, bs, NB, float(scale),
+            _DT[key_cache.dtype], ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
+    else:
+        _check(load().pkv_paged_attention_decode(
+            *ptrs, block_tables.shape[1], *lens_arg, Hq, Hkv, d, bs, NB, float(scale), _DT[key_cache.dtype], ws_ptr,
+            ws_bytes, int(partition_tokens), _stream(q)))
 
 
 def _scales(name, t, Hkv):
@@ -252,7 +264,8 @@ def paged_kv_append_fp8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_s
 
 
 def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq_lens, k_scale, v_scale, scale=None,
-                               max_seq_len=None, workspace=None, partition_tokens=0, planned=False) -> None:
+                               max_seq_len=None, workspace=None, partition_tokens=0, planned=False,
+                               sum_seq_lens=0) -> None:
     """paged_attention_decode over uint8 E4M3 pools: K = e4m3(code) * k_scale[g], V = e4m3(code) * v_scale[g];
     q, out fp16 / bf16 [B, Hq, 128]; k_scale, v_scale float32 [Hkv]."""
     NB, bs, Hkv, d = _pool("key_cache", key_cache, (torch.uint8,))
@@ -274,11 +287,14 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq
         workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
     ws_ptr = _cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    fn = load().pkv_paged_attention_decode_fp8_planned if planned else load().pkv_paged_attention_decode_fp8
-    _check(fn(
-        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
-        NB, float(scale), _DT[q.dtype], _scales("k_scale", k_scale, Hkv), _scales("v_scale", v_scale, Hkv), ws_ptr,
-        ws_bytes, int(partition_tokens), _stream(q)))
+    lens_arg = [ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len)]
+    rest = [Hq, Hkv, d, bs, NB, float(scale), _DT[q.dtype], _scales("k_scale", k_scale, Hkv),
+            _scales("v_scale", v_scale, Hkv), ws_ptr, ws_bytes, int(partition_tokens), _stream(q)]
+    if planned:
+        _check(load().pkv_paged_attention_decode_fp8_planned(*ptrs, block_tables.shape[1], *lens_arg,
+                                                             int(sum_seq_lens), *rest))
+    else:
+        _check(load().pkv_paged_attention_decode_fp8(*ptrs, block_tables.shape[1], *lens_arg, *rest))
 
 
 def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,

@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/pkv.h"
@@ -256,7 +257,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
                           int64_t num_blocks, float scale, pkv_dtype dt, int num_queries, void* workspace,
                           size_t workspace_bytes, int partition_tokens, void* stream, const float* k_scale = nullptr,
                           const float* v_scale = nullptr, pkv::DecodeMode mode = pkv::DecodeMode::kPlanAndRun,
-                          bool kv8_plan = false) {
+                          bool kv8_plan = false, int64_t sum_seq_lens = 0) {
     const bool runs = mode != pkv::DecodeMode::kPlanOnly;
     pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
     if (st != PKV_OK) return st;
@@ -343,7 +344,13 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
                                                 : pkv::decode_ctas_per_sm(head_dim, kv8));
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
-    a.plan_capacity = num_seqs * static_cast<int>(max_parts);
+    // work-list entries the grid covers: every (sequence, partition) the longest sequence
+    // could need, or, with the lengths' sum known, at most B + sum / P entries (a sequence
+    // of length l has max(1, ceil(l / P)) <= 1 + l / P partitions)
+    int64_t capacity = static_cast<int64_t>(num_seqs) * max_parts;
+    if (sum_seq_lens > 0) capacity = std::min(capacity, static_cast<int64_t>(num_seqs) + sum_seq_lens / part);
+    a.plan_capacity = static_cast<int>(capacity);
+    a.sum_seq_lens = sum_seq_lens;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.kv8 = kv8;
     a.k_scale = k_scale;
@@ -381,41 +388,45 @@ pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_
 }
 
 pkv_status pkv_decode_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
-                           int max_seq_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                           pkv_dtype kv_dt, void* workspace, size_t workspace_bytes, int partition_tokens,
-                           void* stream) {
+                           int max_seq_len, int64_t sum_seq_lens, int num_heads, int num_kv_heads, int head_dim,
+                           int block_size, pkv_dtype kv_dt, void* workspace, size_t workspace_bytes,
+                           int partition_tokens, void* stream) {
     if (!valid_dtype(kv_dt) && kv_dt != PKV_E4M3) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(kv_dt));
+    if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(nullptr, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, 1, 1.0f,
                           kv_dt == PKV_E4M3 ? PKV_F16 : kv_dt, 1, workspace, workspace_bytes, partition_tokens,
-                          stream, nullptr, nullptr, pkv::DecodeMode::kPlanOnly, kv_dt == PKV_E4M3);
+                          stream, nullptr, nullptr, pkv::DecodeMode::kPlanOnly, kv_dt == PKV_E4M3, sum_seq_lens);
 }
 
 pkv_status pkv_paged_attention_decode_planned(void* out, const void* q, const void* key_cache,
                                               const void* value_cache, const int32_t* block_tables,
                                               int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
-                                              int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                                              int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
-                                              void* workspace, size_t workspace_bytes, int partition_tokens,
-                                              void* stream) {
+                                              int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                              float scale, pkv_dtype dt, void* workspace, size_t workspace_bytes,
+                                              int partition_tokens, void* stream) {
+    if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
                           workspace, workspace_bytes, partition_tokens, stream, nullptr, nullptr,
-                          pkv::DecodeMode::kRunOnly);
+                          pkv::DecodeMode::kRunOnly, false, sum_seq_lens);
 }
 
 pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void* q, const void* key_cache,
                                                   const void* value_cache, const int32_t* block_tables,
                                                   int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
-                                                  int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                                                  int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                                  int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                                  int num_kv_heads, int head_dim, int block_size,
+                                                  int64_t num_blocks, float scale, pkv_dtype dt,
                                                   const float* k_scale, const float* v_scale, void* workspace,
                                                   size_t workspace_bytes, int partition_tokens, void* stream) {
     if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "k_scale / v_scale are required");
+    if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
                           workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale,
-                          pkv::DecodeMode::kRunOnly);
+                          pkv::DecodeMode::kRunOnly, false, sum_seq_lens);
 }
 
 pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,

@@ -125,10 +125,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
         sGmax[t] = 0;
     }
 
+    // ---- the caller's sum of the lengths, when given, must be the real one (it sized the grid)
+    long long W = 0;
+    if (a.part_auto || a.sum_seq_lens > 0) {
+        W = block_sum(L, next());
+        if (a.sum_seq_lens > 0 && W != a.sum_seq_lens && blockIdx.x == 0 && t == 0) raise_error(a.err, kErrBounds);
+    }
+
     // ---- partition size
     int P = a.part_tokens;
     if (a.part_auto) {
-        const long long W = block_sum(L, next());
         const int lmax = block_max(L, next());
         const long long slots = a.slots > 0 ? a.slots : 1;
         // 0.85 x the positions per slot, counted in 16-bit-pool bytes: an E4M3
@@ -172,6 +178,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
     const int gid = block_scan_max(start ? t : -1, next());
     if (t < B) atomicMax(&sGmax[gid], L);
     const long long n_live = block_sum(np, next());  // its barrier also completes the atomics
+    // more entries than the grid covers (only a wrong sum_seq_lens does this): the rest are
+    // dropped below, and the error word says so
+    if (n_live > a.plan_capacity && blockIdx.x == 0 && t == 0) raise_error(a.err, kErrBounds);
     if (t < B) {
         sNp[t] = np;
         sL[t] = L;

@@ -85,7 +85,8 @@ struct DecodeArgs {
     int part_auto;                   // with a plan: 1 = the plan kernel picks the partition size (>= part_tokens)
     int slots;                       // SMs x resident decode CTAs per SM (for the plan kernel's choice)
     int max_parts;                   // ceil(max_seq_len / part_tokens): the partials' stride
-    int plan_capacity;               // num_seqs * max_parts: entries of `plan` (the grid's work slots)
+    int plan_capacity;               // entries of `plan` the grid covers (<= num_seqs * max_parts)
+    int64_t sum_seq_lens;            // the caller's sum of seq_lens (0: not given); the plan checks it
     float scale_log2;                // scale * log2(e)
     int kv8;                         // 1: the pools hold E4M3 codes (head_dim 128), scaled per KV head
     const float* k_scale;            // [num_kv_heads] (E4M3 pools only)

@@ -25,26 +25,28 @@ def _clean_error_word():
     assert pkv.device_error(reset=True) == 0, "a kernel raised the device error word"
 
 
+@pytest.mark.parametrize("with_sum", [False, True])
 @pytest.mark.parametrize("partition_tokens", [0, 64])
-def test_plan_once_run_every_layer(partition_tokens):
+def test_plan_once_run_every_layer(partition_tokens, with_sum):
     wl = W.build(W.small_spec(num_seqs=6, num_heads=32, num_kv_heads=8, dtype=W.BF16, num_layers=3, seed=701,
                               lens=("fixed", (1500, 33, 700, 1, 2049, 64))))
     step = DeviceStep(wl, partition_tokens=partition_tokens)
     s = wl.spec
+    total = int(wl.seq_lens.sum()) if with_sum else 0       # sizes the grid tighter when given
     pkv.decode_plan(step.workspace, step.block_tables, step.seq_lens, s.num_heads, step.kc[0], wl.max_seq_len,
-                    partition_tokens)
+                    partition_tokens, sum_seq_lens=total)
     planned = []
     for l in range(3):
         pkv.paged_kv_append(step.k_new, step.v_new, step.kc[l], step.vc[l], step.slot_mapping)
         out = torch.empty_like(step.q)
         pkv.paged_attention_decode(out, step.q, step.kc[l], step.vc[l], step.block_tables, step.seq_lens, wl.scale,
                                    max_seq_len=wl.max_seq_len, workspace=step.workspace,
-                                   partition_tokens=partition_tokens, planned=True)
+                                   partition_tokens=partition_tokens, planned=True, sum_seq_lens=total)
         planned.append(out)
     again = torch.empty_like(step.q)                 # the same plan once more: tickets were reset
     pkv.paged_attention_decode(again, step.q, step.kc[2], step.vc[2], step.block_tables, step.seq_lens, wl.scale,
                                max_seq_len=wl.max_seq_len, workspace=step.workspace,
-                               partition_tokens=partition_tokens, planned=True)
+                               partition_tokens=partition_tokens, planned=True, sum_seq_lens=total)
     for l in range(3):                               # the single call (its own plan) on each layer
         step.decode(l)
     torch.cuda.synchronize()
@@ -118,6 +120,35 @@ def test_full_grid_batch_plans_nothing_and_runs():
     pkv.paged_attention_decode(out, step.q, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
                                max_seq_len=wl.max_seq_len, workspace=step.workspace, partition_tokens=64,
                                planned=True)
+    torch.cuda.synchronize()
+    kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
+    ref = oracle.attention_ref(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
+    assert max_abs_err(out, ref) <= TOL[s.dtype]
+
+
+def test_wrong_length_sum_is_flagged():
+    """A sum_seq_lens below the real sum sizes the grid too small: the plan flags it (and
+    drops the entries past the grid, never writing out of range)."""
+    wl = W.build(W.small_spec(num_seqs=8, num_heads=16, num_kv_heads=4, seed=705,
+                              lens=("fixed", (3000, 2500, 40, 900, 1200, 5, 64, 2047))))
+    step = DeviceStep(wl, partition_tokens=64)
+    s = wl.spec
+    pkv.paged_kv_append(step.k_new, step.v_new, step.kc[0], step.vc[0], step.slot_mapping)
+    wrong = int(wl.seq_lens.sum()) // 4
+    pkv.decode_plan(step.workspace, step.block_tables, step.seq_lens, s.num_heads, step.kc[0], wl.max_seq_len, 64,
+                    sum_seq_lens=wrong)
+    out = torch.empty_like(step.q)
+    pkv.paged_attention_decode(out, step.q, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
+                               max_seq_len=wl.max_seq_len, workspace=step.workspace, partition_tokens=64,
+                               planned=True, sum_seq_lens=wrong)
+    torch.cuda.synchronize()
+    assert pkv.device_error(reset=True) & 1, "a wrong length sum must raise the bounds bit"
+    # planned again with the right sum, the same workspace gives the right answer
+    pkv.decode_plan(step.workspace, step.block_tables, step.seq_lens, s.num_heads, step.kc[0], wl.max_seq_len, 64,
+                    sum_seq_lens=int(wl.seq_lens.sum()))
+    pkv.paged_attention_decode(out, step.q, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
+                               max_seq_len=wl.max_seq_len, workspace=step.workspace, partition_tokens=64,
+                               planned=True, sum_seq_lens=int(wl.seq_lens.sum()))
     torch.cuda.synchronize()
     kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
     ref = oracle.attention_ref(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
