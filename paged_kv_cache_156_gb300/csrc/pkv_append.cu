@@ -18,8 +18,10 @@ namespace {
 constexpr int kWarpsPerBlock = 4;
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendArgs a) {
-    // a following decode call's plan kernel may start launching; it waits for
-    // this grid to finish before it reads anything
+    // This grid may have launched early: it waits for the previous one before
+    // touching memory; then the next kernel (a plan or decode grid, which waits
+    // for this one) may start launching.
+    grid_dependency_wait();
     launch_dependents();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -68,6 +70,7 @@ __device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_fp8_kernel(const AppendFp8Args a) {
+    grid_dependency_wait();
     launch_dependents();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -90,23 +93,33 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_fp8_kernel(const A
         vd[i] = quantize8<BF16>(y, __ldg(a.v_scale + h));
     }
 }
+
+// Launched with programmatic stream serialization: the grid may become
+// resident while the previous kernel (a decode) finishes, and waits for it.
+template <typename Kern, typename Args>
+cudaError_t launch_dependent(Kern kern, const Args& a, int64_t tokens, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((tokens + kWarpsPerBlock - 1) / kWarpsPerBlock));
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
 }  // namespace
 
 cudaError_t launch_append_fp8(const AppendFp8Args& a, cudaStream_t s) {
     if (a.num_tokens <= 0) return cudaSuccess;
-    const int64_t blocks = (a.num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (a.bf16)
-        append_fp8_kernel<true><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, s>>>(a);
-    else
-        append_fp8_kernel<false><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return a.bf16 ? launch_dependent(append_fp8_kernel<true>, a, a.num_tokens, s)
+                  : launch_dependent(append_fp8_kernel<false>, a, a.num_tokens, s);
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
     if (a.num_tokens <= 0) return cudaSuccess;
-    const int64_t blocks = (a.num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    append_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(append_kernel, a, a.num_tokens, s);
 }
 
 }  // namespace pkv

@@ -301,6 +301,10 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         return;
     }
 
+    // this CTA's main loop is done: the next kernel in the stream (an append,
+    // which waits for this grid) may start launching as the grid drains
+    if (threadIdx.x == 0) launch_dependents();
+
     // ================================================= epilogue
     // merge the warps' states through shared memory (the ring is free: every
     // chunk was consumed by every warp, so no copy is still landing)

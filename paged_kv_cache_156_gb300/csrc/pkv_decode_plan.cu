@@ -106,8 +106,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeArgs a) 
     const int nh = a.num_kv_heads * a.head_groups;
     int nb = 0;                                     // next reduction buffer
     auto next = [&]() { long long* b = buf[nb]; nb ^= 1; return b; };
-    launch_dependents();                            // the decode grid may launch now; it waits for this grid
     grid_dependency_wait();                         // lengths and tables may come from the previous kernel
+    launch_dependents();                            // the decode grid may launch now; it waits for this grid
 
     // ---- this thread's sequence: length (clamped to [0, max_seq_len]) and first block
     int L = 0, b0 = -1;

@@ -341,6 +341,8 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
         return;
     }
 
+    if (threadIdx.x == 0) launch_dependents();      // the main loop is done: the next kernel may launch
+
     // ================================================= epilogue: this warp's rows are complete
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
