@@ -21,7 +21,6 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
-import functools
 import hashlib
 import json
 import math
@@ -56,6 +55,8 @@ def parse_args():
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
     p.add_argument("--ref-seconds", type=float, default=90.0, help="total budget of the --impl reference run")
+    p.add_argument("--separate-append", action="store_true",
+                   help="launch paged_kv_append and the decode separately instead of the fused call")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -285,11 +286,14 @@ def run_pkv(args, rank, world, local):
     planned = spec.num_seqs <= pkv.PLAN_MAX_SEQS
     max_parts_min = math.ceil(wl.max_seq_len / part_min) if wl.max_seq_len else 1
     # A step plans once (the batch is the same in every layer: lengths and block tables do not
-    # depend on this step's slot writes), right after layer 0's append, whose grid lets the plan
-    # launch early; every layer then decodes over the plan.  The decode events time the decode
-    # kernel alone; the step value counts the plan too.
+    # depend on this step's slot writes); every layer then writes its new tokens and decodes over
+    # the plan.  With one new token per sequence (decode proper) the slot write rides in the decode
+    # launch (pkv_paged_kv_append_decode); a step that writes more slots per sequence (the rest of a
+    # copied block) launches paged_kv_append first.  The decode events time the decode kernel
+    # alone; the step value counts the plan too.
+    fused = wl.num_tokens == spec.num_seqs and not args.separate_append
     launches_per_step = (1 if len(wl.copy_pairs) else 0) + (1 if planned else 0) + spec.num_layers * (
-        2 + (0 if planned or max_parts_min == 1 else 1))
+        (1 if fused else 2) + (0 if planned or max_parts_min == 1 else 1))
 
     total_len = int(wl.seq_lens.sum())             # the scheduler knows it; it sizes the decode grid
     ev_pairs = []
@@ -298,23 +302,37 @@ def run_pkv(args, rank, world, local):
         kcs, vcs = pools[i % replicas]
         if len(wl.copy_pairs):
             pkv.copy_blocks(kcs, vcs, pairs)
+        if fused:
+            pkv.decode_plan(ws, tables, lens, spec.num_heads, kcs[0], wl.max_seq_len, args.partition_tokens,
+                            sum_seq_lens=total_len)
         for l in range(spec.num_layers):
-            if spec.fp8:
-                pkv.paged_kv_append_fp8(k_new, v_new, kcs[l], vcs[l], slots, k_scales[l], v_scales[l])
-            else:
-                pkv.paged_kv_append(k_new, v_new, kcs[l], vcs[l], slots)
-            if l == 0:
-                pkv.decode_plan(ws, tables, lens, spec.num_heads, kcs[0], wl.max_seq_len, args.partition_tokens,
-                                sum_seq_lens=total_len)
-            rec = timed and l == 0
-            if rec:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if not fused:
+                if spec.fp8:
+                    pkv.paged_kv_append_fp8(k_new, v_new, kcs[l], vcs[l], slots, k_scales[l], v_scales[l])
+                else:
+                    pkv.paged_kv_append(k_new, v_new, kcs[l], vcs[l], slots)
+                if l == 0:
+                    pkv.decode_plan(ws, tables, lens, spec.num_heads, kcs[0], wl.max_seq_len, args.partition_tokens,
+                                    sum_seq_lens=total_len)
+            # decode events: around layer 0's launch, or, for a fused multi-layer step, around
+            # layers 1 .. L-1 (back-to-back decode launches, nothing else in between)
+            chain = fused and spec.num_layers > 1
+            rec = timed and (l == 0 if not chain else l == spec.num_layers - 1)
+            if timed and (l == 0 if not chain else l == 1):
+                a = torch.cuda.Event(enable_timing=True)
                 a.record()
-            decode = (functools.partial(pkv.paged_attention_decode_fp8, k_scale=k_scales[l], v_scale=v_scales[l])
-                      if spec.fp8 else pkv.paged_attention_decode)
-            decode(outs[l], q, kcs[l], vcs[l], tables, lens, scale=wl.scale, max_seq_len=wl.max_seq_len,
-                   workspace=ws, partition_tokens=args.partition_tokens, planned=True, sum_seq_lens=total_len)
+            kw = dict(scale=wl.scale, max_seq_len=wl.max_seq_len, workspace=ws, partition_tokens=args.partition_tokens,
+                      planned=True, sum_seq_lens=total_len)
+            if fused:
+                if spec.fp8:
+                    kw.update(k_scale=k_scales[l], v_scale=v_scales[l])
+                pkv.paged_kv_append_decode(outs[l], q, k_new, v_new, kcs[l], vcs[l], slots, tables, lens, **kw)
+            elif spec.fp8:
+                pkv.paged_attention_decode_fp8(outs[l], q, kcs[l], vcs[l], tables, lens, k_scales[l], v_scales[l], **kw)
+            else:
+                pkv.paged_attention_decode(outs[l], q, kcs[l], vcs[l], tables, lens, **kw)
             if rec:
+                b = torch.cuda.Event(enable_timing=True)
                 b.record()
                 ev_pairs.append((a, b))
 
@@ -341,12 +359,15 @@ def run_pkv(args, rank, world, local):
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
     max_ms = max_over_ranks(elapsed_ms, world)
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_pairs]))
+    dec_launches = spec.num_layers - 1 if (fused and spec.num_layers > 1) else 1
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_pairs])) / dec_launches
     assert pkv.device_error() == 0, "device error word raised during the timed region"
 
     value = world * nbytes["step"] * args.steps / (max_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
-    dec_gbs = nbytes["decode_unique"] / (dec_ms / 1e3) / 1e9
+    # the timed launch moves the decode's bytes, plus the slot write's when it is fused in
+    kernel_bytes = nbytes["decode_unique"] + (nbytes["append"] if fused else 0)
+    dec_gbs = kernel_bytes / (dec_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
 
     # ---- end to end: inputs from pinned host memory, outputs read back, every step
@@ -428,16 +449,21 @@ def run_pkv(args, rank, world, local):
                    "num_blocks": wl.num_blocks, "copy_pairs": int(len(wl.copy_pairs)),
                    "partition_tokens": part, "partition_tokens_min": part_min, "max_partitions": max_parts,
                    "work_list": "plan kernel" if planned else "full grid",
+                   "slot_write": "fused into the decode launch" if fused else "paged_kv_append launch",
                    "l2": f"inputs larger than L2: {replicas} rotating pool replicas of "
                          f"{footprint / 1e9:.3f} GB each (L2 {L2_BYTES / 2**20:.0f} MiB)",
                    "parallelism": f"replicas x{world} (no data-path collective)"},
         "tokens_per_s": round(world * spec.num_seqs * args.steps / (max_ms / 1e3), 1),
         "step_bytes": nbytes,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel (planned run of layer 0, in-kernel split-K merge; "
-                                               "the step's one plan kernel is outside this timing, inside value)",
+        "roofline": {"bound": "hbm", "kernel": ("decode_kernel (" +
+                                                (f"mean of layers 1..{spec.num_layers - 1}, launched back to back"
+                                                 if dec_launches > 1 else "planned run of layer 0") +
+                                                ", in-kernel split-K merge" +
+                                                (", slot write fused in" if fused else "") +
+                                                "; the step's one plan kernel is outside this timing, inside value)"),
                      "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": nbytes["decode_unique"], "avg_launch_ms": round(dec_ms, 5)},
+                     "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 5)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

@@ -229,6 +229,43 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void*
                                                   size_t workspace_bytes, int partition_tokens, void* stream);
 
 /*
+ * paged_kv_append + paged_attention_decode in one launch.
+ *
+ * P2 §2.3 and P1 §4.2.2 (each step's new token goes into the slot the block
+ * manager gave it, and the step then attends over the sequence including that
+ * token).  Same results as pkv_paged_kv_append (pkv_paged_kv_append_fp8 for
+ * kv_dt == PKV_E4M3) of token s = 0 .. num_seqs - 1 followed by
+ * pkv_paged_attention_decode (_fp8; _planned when `planned` is non-zero, over
+ * the plan pkv_decode_plan wrote), bit for bit in the caches, without the
+ * separate slot-write launch: the decode CTA that reads position
+ * seq_lens[s] - 1 writes the token there itself before its tile loads.
+ *
+ *   k, v          [num_seqs][num_kv_heads][head_dim] in dtype `dt` (q's)
+ *   slot_mapping  int64 [num_seqs]: the slot of position seq_lens[s] - 1 of
+ *                 sequence s (block_tables[s][(seq_lens[s]-1) / block_size] *
+ *                 block_size + (seq_lens[s]-1) % block_size), or negative for
+ *                 a sequence with no new token (nothing is written)
+ *   kv_dt         dt for 16-bit pools, PKV_E4M3 for 8-bit pools (then
+ *                 k_scale / v_scale as in pkv_paged_kv_append_fp8; else
+ *                 ignored)
+ *   other arguments as pkv_paged_attention_decode / _planned.
+ * A non-negative slot that is not that position's slot (or a sequence of
+ * length 0 with one) is not written and raises the error word's bounds bit.
+ * The block holding position seq_lens[s] - 1 must not be read by another
+ * sequence of the call (the block manager's copy-on-write gives every
+ * sequence its own last block before it appends).
+ */
+PKV_API pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const void* k, const void* v,
+                                      void* key_cache, void* value_cache, const int64_t* slot_mapping,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                      int64_t sum_seq_lens, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
+                                      pkv_dtype kv_dt, const float* k_scale, const float* v_scale,
+                                      void* workspace, size_t workspace_bytes, int partition_tokens,
+                                      int planned, void* stream);
+
+/*
  * paged_attention_verify -- num_queries query tokens per sequence over its
  * paged K/V, causal among themselves (the verification step of speculative
  * decoding).

@@ -32,7 +32,7 @@ ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_deco
                "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
                "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables", "pkv_paged_kv_append_fp8",
                "pkv_paged_attention_decode_fp8", "pkv_decode_plan", "pkv_paged_attention_decode_planned",
-               "pkv_paged_attention_decode_fp8_planned")
+               "pkv_paged_attention_decode_fp8_planned", "pkv_paged_kv_append_decode")
 
 _lib = None
 
@@ -82,6 +82,9 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode_planned.restype = c_i
     lib.pkv_paged_attention_decode_planned.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i,
                                                        c_i, c_i, c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_paged_kv_append_decode.restype = c_i
+    lib.pkv_paged_kv_append_decode.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i,
+                                               c_i, c_i, c_i, c_i64, c_f, c_i, c_i, c_p, c_p, c_p, c_sz, c_i, c_i, c_p]
     lib.pkv_decode_plan.restype = c_i
     lib.pkv_decode_plan.argtypes = [c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i, c_i, c_i, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_copy_blocks.restype = c_i
@@ -295,6 +298,46 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq
                                                              int(sum_seq_lens), *rest))
     else:
         _check(load().pkv_paged_attention_decode_fp8(*ptrs, block_tables.shape[1], *lens_arg, *rest))
+
+
+def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, block_tables, seq_lens, scale=None,
+                           max_seq_len=None, workspace=None, partition_tokens=0, planned=False, sum_seq_lens=0,
+                           k_scale=None, v_scale=None) -> None:
+    """paged_kv_append of one new token per sequence (k, v [B, Hkv, d]; slot_mapping int64 [B], the slot of
+    position seq_lens[s] - 1, or < 0 for none) then paged_attention_decode, in one launch.  uint8 pools hold
+    E4M3 codes and take k_scale / v_scale as paged_kv_append_fp8 does."""
+    kv8 = key_cache.dtype == torch.uint8
+    NB, bs, Hkv, d = _pool("key_cache", key_cache, tuple(_POOL_DT))
+    if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
+        raise ValueError("value_cache must match key_cache")
+    B, Hq, dq = q.shape
+    if dq != d or tuple(out.shape) != (B, Hq, d):
+        raise ValueError("q and out must be [B, num_heads, head_dim]")
+    if tuple(k.shape) != (B, Hkv, d) or tuple(v.shape) != (B, Hkv, d):
+        raise ValueError("k and v must be [B, num_kv_heads, head_dim]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    qdt = (torch.float16, torch.bfloat16) if kv8 else key_cache.dtype
+    ptrs = [_cuda("out", out, qdt), _cuda("q", q, out.dtype), _cuda("k", k, out.dtype, 3), _cuda("v", v, out.dtype, 3),
+            _cuda("key_cache", key_cache), _cuda("value_cache", value_cache),
+            _cuda("slot_mapping", slot_mapping, torch.int64, 1), _cuda("block_tables", block_tables, torch.int32, 2)]
+    _cuda("seq_lens", seq_lens, torch.int32, 1)
+    if block_tables.shape[0] != B or seq_lens.shape[0] != B or slot_mapping.shape[0] != B:
+        raise ValueError("block_tables / seq_lens / slot_mapping batch mismatch")
+    if kv8:
+        scales = [_scales("k_scale", k_scale, Hkv), _scales("v_scale", v_scale, Hkv)]
+    else:
+        scales = [None, None]
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
+    ws_ptr = _cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_kv_append_decode(
+        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), int(sum_seq_lens),
+        Hq, Hkv, d, bs, NB, float(scale), _DT[q.dtype], _POOL_DT[key_cache.dtype], *scales, ws_ptr, ws_bytes,
+        int(partition_tokens), int(bool(planned)), _stream(q)))
 
 
 def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,

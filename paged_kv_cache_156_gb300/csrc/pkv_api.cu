@@ -247,6 +247,13 @@ int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, i
 
 namespace {
 
+// The new tokens of a fused slot write + decode call (one per sequence).
+struct NewTokens {
+    const void* k;
+    const void* v;
+    const int64_t* slot_mapping;
+};
+
 // Decode (num_queries == 1) and multi-query verify share one path: a KV head
 // serves (num_heads / num_kv_heads) * num_queries query rows.  `mode`: plan
 // and run (one call), plan only (pkv_decode_plan; q, out and the pools are
@@ -257,7 +264,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
                           int64_t num_blocks, float scale, pkv_dtype dt, int num_queries, void* workspace,
                           size_t workspace_bytes, int partition_tokens, void* stream, const float* k_scale = nullptr,
                           const float* v_scale = nullptr, pkv::DecodeMode mode = pkv::DecodeMode::kPlanAndRun,
-                          bool kv8_plan = false, int64_t sum_seq_lens = 0) {
+                          bool kv8_plan = false, int64_t sum_seq_lens = 0, const NewTokens* fused = nullptr) {
     const bool runs = mode != pkv::DecodeMode::kPlanOnly;
     pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
     if (st != PKV_OK) return st;
@@ -287,6 +294,13 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
             return fail(PKV_ERR_INVALID, "k_scale / v_scale must be 4-byte aligned");
         if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
             return fail(PKV_ERR_INVALID, "out, q and caches must be 16-byte aligned");
+        if (fused) {
+            if (num_queries != 1) return fail(PKV_ERR_INVALID, "a fused slot write decodes one query token");
+            if (!fused->k || !fused->v || !fused->slot_mapping) return fail(PKV_ERR_INVALID, "null pointer");
+            if (!aligned16(fused->k) || !aligned16(fused->v) ||
+                (reinterpret_cast<uintptr_t>(fused->slot_mapping) & 7u))
+                return fail(PKV_ERR_INVALID, "k and v must be 16-byte aligned (slot_mapping 8-byte)");
+        }
     }
 
     const int dev = current_device();
@@ -355,6 +369,13 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.kv8 = kv8;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    if (runs && fused) {
+        a.k_new = static_cast<const uint4*>(fused->k);
+        a.v_new = static_cast<const uint4*>(fused->v);
+        a.slot_mapping = fused->slot_mapping;
+        a.key_cache = const_cast<void*>(key_cache);
+        a.value_cache = const_cast<void*>(value_cache);
+    }
     cudaError_t e = verify_kernel ? pkv::launch_verify(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
                                                        static_cast<cudaStream_t>(stream), mode)
                                   : pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
@@ -439,6 +460,29 @@ pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* 
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
                           workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale);
+}
+
+pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const void* k, const void* v, void* key_cache,
+                                      void* value_cache, const int64_t* slot_mapping, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                      int64_t sum_seq_lens, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt, pkv_dtype kv_dt,
+                                      const float* k_scale, const float* v_scale, void* workspace,
+                                      size_t workspace_bytes, int partition_tokens, int planned, void* stream) {
+    if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
+    if (kv_dt == PKV_E4M3) {
+        if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "E4M3 pools need k_scale and v_scale");
+    } else if (kv_dt != dt) {
+        return fail(PKV_ERR_INVALID, "kv_dt must be dt or PKV_E4M3");
+    } else {
+        k_scale = v_scale = nullptr;
+    }
+    const NewTokens nt{k, v, slot_mapping};
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
+                          workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale,
+                          planned ? pkv::DecodeMode::kRunOnly : pkv::DecodeMode::kPlanAndRun, false, sum_seq_lens,
+                          &nt);
 }
 
 pkv_status pkv_paged_kv_append_fp8(const void* k, const void* v, void* key_cache, void* value_cache,

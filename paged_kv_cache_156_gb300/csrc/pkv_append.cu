@@ -47,27 +47,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
 // ---------------------------------------------------------------- E4M3 pools
 // The same scatter into an 8-bit pool (the KV quantization of "LLM 推理优化深度实战"
 // §6.2: attention then reads low-precision K/V).  Each lane converts 8
-// elements per step: float32, divided by its KV head's scale (IEEE division),
-// rounded to the nearest E4M3 code (ties to even) with saturation at 448.
-template <bool BF16>
-__device__ __forceinline__ float2 pair_to_float2(uint32_t x) {
-    if constexpr (BF16) return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-    else return __half22float2(*reinterpret_cast<const __half2*>(&x));
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
-    uint32_t w[4];
-    const uint32_t in[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = pair_to_float2<BF16>(in[i]);
-        w[i] = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale)), __NV_SATFINITE,
-                                        __NV_E4M3);
-    }
-    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-}
-
+// elements per step with quantize8 (pkv_device.cuh).
 template <bool BF16>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_fp8_kernel(const AppendFp8Args a) {
     grid_dependency_wait();

@@ -41,6 +41,8 @@
 //    up raises the error word and the CTA winds down.
 #include <stdlib.h>
 
+#include <type_traits>
+
 #include "pkv_decode_common.cuh"
 
 namespace pkv {
@@ -140,12 +142,27 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     dec::WarpState<D> ws;
     const int first_blk = start / bs;
     const int tcount = min(P / bs, a.max_blocks_per_seq - first_blk);
+    // Fused slot write: the new token's row (K in the first D/8 lanes, V in the
+    // next D/8, 16 bytes each) for a CTA that may hold position seq_len - 1.
+    constexpr int kHV = D / 8;
+    uint4 nrow = make_uint4(0u, 0u, 0u, 0u);
+    int64_t nslot = -1;
+    float nscale = 1.0f;
+    const bool maybe_put = !MQ && a.k_new != nullptr && (Lp <= 0 || part == (Lp + P - 1) / P - 1);
     if (warp == CW) {
         const int32_t* row = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + first_blk;
 #pragma unroll
         for (int k = 0; k < kTePerLane; ++k) {
             const int i = lane + 32 * k;
             te[k] = (32 * k < tcount && i < tcount) ? __ldg(row + i) : 0;
+        }
+        if (maybe_put) {
+            nslot = __ldg(a.slot_mapping + s);
+            if (lane < 2 * kHV) {
+                const uint4* src = lane < kHV ? a.k_new : a.v_new;
+                nrow = __ldg(src + (static_cast<int64_t>(s) * a.num_kv_heads + kvh) * kHV + lane % kHV);
+                if constexpr (KV8) nscale = __ldg((lane < kHV ? a.k_scale : a.v_scale) + kvh);
+            }
         }
     } else if constexpr (KV8) {
         // Q^T in consume_chunk_fp8's order: lane holds q[n = lane/4][32*t + 4*ks + {0,1}]
@@ -183,6 +200,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         }
     }
     if (L <= 0) {                                   // empty sequence: zeros
+        // a fused slot write needs a position for its token
+        if (maybe_put && warp == CW && lane == 0 && part == 0 && hh == 0 && nslot >= 0) raise_error(a.err, kErrBounds);
         if (part == 0)
             for (int i = threadIdx.x; i < gc * D; i += kThreads)
                 out[dec::qo_row<MQ>(a, sh0, s, kvh, vh0, i / D) * D + i % D] = T(0.0f);
@@ -224,17 +243,43 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
             }
         }
         __syncwarp();
-        if (lane == 0 && !*abort_flag) {
+        // The fused slot write goes to the slot of position L - 1, which only
+        // this partition reads in this call (and any other head group of the
+        // same KV head, which writes the same bytes); anything else is refused.
+        bool put = false;
+        if (maybe_put && part == nparts - 1 && nslot >= 0) {
+            const int pb = tbl[(L - 1) / bs - first_blk];
+            put = pb >= 0 && nslot == static_cast<int64_t>(pb) * bs + (L - 1) % bs;
+            if (!put && lane == 0) raise_error(a.err, kErrBounds);
+        }
+        if (*abort_flag) return;
+        if (lane == 0) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-            const int per_chunk = kChunk / bs;
-            for (int c = 0; c < nchunks; ++c) {
-                const int st = c % STAGES;
-                const unsigned ph = (c / STAGES) & 1;
-                if (!dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
-                    dec::raise_abort(a.err, abort_flag);
-                    break;
+        }
+        const int per_chunk = kChunk / bs;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % STAGES;
+            const unsigned ph = (c / STAGES) & 1;
+            if (put && c == nchunks - 1) {          // the chunk holding position L - 1
+                if (lane < 2 * kHV) {
+                    const int64_t at = (nslot * a.num_kv_heads + kvh) * kHV + lane % kHV;
+                    if constexpr (KV8)
+                        reinterpret_cast<uint2*>(lane < kHV ? a.key_cache : a.value_cache)[at] =
+                            quantize8<std::is_same<T, __nv_bfloat16>::value>(nrow, nscale);
+                    else
+                        reinterpret_cast<uint4*>(lane < kHV ? a.key_cache : a.value_cache)[at] = nrow;
                 }
+                fence_proxy_async_global();         // the tile loads below see these bytes
+                __syncwarp();
+            }
+            bool got = dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag);
+            got = __all_sync(0xffffffffu, got);
+            if (!got) {
+                if (lane == 0) dec::raise_abort(a.err, abort_flag);
+                break;
+            }
+            if (lane == 0) {
                 const int tok0 = start + c * kChunk;
                 const int nb = (min(end, tok0 + kChunk) - tok0 + bs - 1) / bs;
                 mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * kEB * 2));
@@ -248,6 +293,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
                     }
                 }
             }
+            __syncwarp();
         }
         return;
     }

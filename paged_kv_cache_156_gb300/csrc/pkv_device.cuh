@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace pkv {
@@ -47,6 +48,12 @@ __device__ __forceinline__ void fence_barrier_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy global writes before its later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -198,6 +205,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---------------------------------------------------------------- E4M3 codes
+// Eight fp16 / bf16 elements to eight E4M3 codes: float32(x) / float32(scale)
+// (IEEE division), rounded to the nearest code (ties to even), saturating at
+// +-448.  Used by every kernel that writes an E4M3 pool, so all of them store
+// the same codes for the same token.
+template <bool BF16>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t x) {
+    if constexpr (BF16) return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+    else return __half22float2(*reinterpret_cast<const __half2*>(&x));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
+    uint32_t w[4];
+    const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = pair_to_float2<BF16>(in[i]);
+        w[i] = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale)), __NV_SATFINITE,
+                                        __NV_E4M3);
+    }
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bit) {

@@ -91,6 +91,15 @@ struct DecodeArgs {
     int kv8;                         // 1: the pools hold E4M3 codes (head_dim 128), scaled per KV head
     const float* k_scale;            // [num_kv_heads] (E4M3 pools only)
     const float* v_scale;
+    // Fused slot write (decode only; nullptr k_new: none).  Before attending,
+    // the CTA whose partition holds position seq_len - 1 of sequence s writes
+    // that sequence's new token (k_new / v_new row s, quantized for an E4M3
+    // pool) into slot_mapping[s], which must be that position's slot.
+    const uint4* k_new = nullptr;    // [B][num_kv_heads][D] in the query dtype
+    const uint4* v_new = nullptr;
+    const int64_t* slot_mapping = nullptr;   // [B]
+    void* key_cache = nullptr;       // the pools written by the fused slot write
+    void* value_cache = nullptr;
 };
 
 // Sequences a call plans (sorts and compacts) at most; larger batches run the
