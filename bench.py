@@ -632,7 +632,9 @@ def run_verify(args, rank, world, local):
     q = torch.randn((B, nq, Hq, d), generator=g, device=dev, dtype=torch.float32).to(tdt)
     out = torch.empty_like(q)
     tables = torch.from_numpy(wl.block_tables).to(dev)
-    lens = torch.from_numpy(np.maximum(wl.seq_lens, nq)).to(dev)
+    lens_h = np.maximum(wl.seq_lens, nq)
+    lens = torch.from_numpy(lens_h).to(dev)
+    total_len = int(lens_h.sum())                   # sizes the grid
     footprint = wl.pool_bytes_per_layer()
     replicas = max(2, min(4, math.ceil(3 * L2_BYTES / footprint)))
     pools = [W.device_pools(wl, 0, dev) for _ in range(replicas)]
@@ -647,7 +649,7 @@ def run_verify(args, rank, world, local):
     def call(i):
         k, v = pools[i % replicas]
         pkv.paged_attention_verify(out, q, k, v, tables, lens, wl.scale, max_seq_len=wl.max_seq_len, workspace=ws,
-                                   partition_tokens=args.partition_tokens)
+                                   partition_tokens=args.partition_tokens, sum_seq_lens=total_len)
 
     for i in range(max(3, args.warmup)):
         call(i)

@@ -284,13 +284,15 @@ PKV_API pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const vo
  *                 num_kv_heads, head_dim, max_seq_len, partition_tokens) bytes
  *   num_queries   in [1, 64]; seq_lens[s] should be 0 or >= num_queries (a
  *                 query token that sees no position gets a zero output)
+ *   sum_seq_lens  the sum of seq_lens if known, else 0; it only sizes the
+ *                 grid, as for pkv_paged_attention_decode_planned
  */
 PKV_API pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_cache,
                                       const void* value_cache, const int32_t* block_tables,
                                       int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
-                                      int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
-                                      int num_queries, void* workspace, size_t workspace_bytes,
+                                      int max_seq_len, int64_t sum_seq_lens, int num_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int64_t num_blocks, float scale,
+                                      pkv_dtype dt, int num_queries, void* workspace, size_t workspace_bytes,
                                       int partition_tokens, void* stream);
 
 /*

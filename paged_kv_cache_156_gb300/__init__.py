@@ -68,8 +68,8 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
                                                c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_paged_attention_verify.restype = c_i
-    lib.pkv_paged_attention_verify.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i, c_i, c_i, c_i,
-                                               c_i64, c_f, c_i, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_paged_attention_verify.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i, c_i,
+                                               c_i, c_i64, c_f, c_i, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_paged_kv_append_fp8.restype = c_i
     lib.pkv_paged_kv_append_fp8.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i, c_i, c_i, c_i, c_p, c_p, c_p]
     lib.pkv_paged_attention_decode_fp8.restype = c_i
@@ -341,7 +341,7 @@ def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, b
 
 
 def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,
-                           workspace=None, partition_tokens=0) -> None:
+                           workspace=None, partition_tokens=0, sum_seq_lens=0) -> None:
     """Multi-query paged attention: q, out [B, nq, Hq, d]; query token i of sequence s attends over
     positions [0, seq_lens[s] - nq + i] (the last nq positions are the queries' own K/V)."""
     NB, bs, Hkv, d = _pool("key_cache", key_cache)
@@ -366,8 +366,9 @@ def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_len
     ws_ptr = _cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().pkv_paged_attention_verify(
-        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), Hq, Hkv, d, bs,
-        NB, float(scale), _DT[key_cache.dtype], nq, ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
+        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), int(sum_seq_lens),
+        Hq, Hkv, d, bs, NB, float(scale), _DT[key_cache.dtype], nq, ws_ptr, ws_bytes, int(partition_tokens),
+        _stream(q)))
 
 
 def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:

@@ -354,7 +354,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.block_size = block_size;
     a.part_tokens = part;
     a.part_auto = partition_tokens == 0;
-    a.slots = sm_count_of(dev) * (verify_kernel ? pkv::verify_ctas_per_sm(head_dim)
+    a.slots = sm_count_of(dev) * (verify_kernel ? pkv::verify_ctas_per_sm(head_dim, a.group)
                                                 : pkv::decode_ctas_per_sm(head_dim, kv8));
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
@@ -400,12 +400,15 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
 
 pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_cache, const void* value_cache,
                                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
-                                      int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
-                                      int block_size, int64_t num_blocks, float scale, pkv_dtype dt, int num_queries,
-                                      void* workspace, size_t workspace_bytes, int partition_tokens, void* stream) {
+                                      int num_seqs, int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+                                      pkv_dtype dt, int num_queries, void* workspace, size_t workspace_bytes,
+                                      int partition_tokens, void* stream) {
+    if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt,
-                          num_queries, workspace, workspace_bytes, partition_tokens, stream);
+                          num_queries, workspace, workspace_bytes, partition_tokens, stream, nullptr, nullptr,
+                          pkv::DecodeMode::kPlanAndRun, false, sum_seq_lens);
 }
 
 pkv_status pkv_decode_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,

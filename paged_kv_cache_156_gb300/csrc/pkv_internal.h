@@ -137,7 +137,7 @@ constexpr int kVerifyMinRows = 16;
 constexpr int kVerifyRowsPerCta = 64;
 cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
                           int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
-int verify_ctas_per_sm(int head_dim);
+int verify_ctas_per_sm(int head_dim, int rows);   // rows: query rows per KV head
 
 // CTAs of the decode kernel resident per SM on the current device (current
 // configuration; kv8: the E4M3-pool kernel), or 0 if it cannot be queried.

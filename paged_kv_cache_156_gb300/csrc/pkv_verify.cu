@@ -15,9 +15,13 @@
 // K fragments from the same TMA ring as decode (ldmatrix), an fp32 online
 // softmax per row, and O[16 x d] += P V with P taken straight from the S
 // accumulators (the accumulator layout of S is the A-operand layout of P)
-// and V fragments by ldmatrix.trans.  A warp owns whole rows, so its rows
-// need no merge across warps; split partitions merge through the workspace
-// with the same ticket protocol as decode (the last partition merges).
+// and V fragments by ldmatrix.trans.  With more than 32 rows a warp owns whole
+// rows for the whole chunk.  With at most 32 (GQA 8 and four draft tokens,
+// say) the two warps of a 16-row tile split each chunk's positions, 32 each,
+// so all four warps work; each keeps its own online softmax and the pair
+// merges lane by lane through shared memory after the last chunk.  Split
+// partitions merge through the workspace with the same ticket protocol as
+// decode (the last partition merges).
 #include <stdlib.h>
 
 #include "pkv_decode_common.cuh"
@@ -50,7 +54,9 @@ __device__ __forceinline__ int64_t vrow_offset(const DecodeArgs& a, int s, int k
     return (static_cast<int64_t>(s) * a.num_queries + i) * a.num_heads + kvh * a.qgroup + hl;
 }
 
-template <typename T, int D>
+// SPLIT: warps sharing one 16-row tile (1: 64 rows per CTA; 2: 32 rows, each
+// warp takes half of every chunk's positions).
+template <typename T, int D, int SPLIT>
 __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                           const __grid_constant__ CUtensorMap tmv,
                                                                           const DecodeArgs a) {
@@ -58,7 +64,8 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
     using S = VSmem<D>;
     using M = Mma<T>;
     constexpr int kChunk = G::kChunk;               // 64 positions
-    constexpr int kNT = kChunk / 8;                 // n-tiles of S per chunk
+    constexpr int kNT = kChunk / 8 / SPLIT;         // n-tiles of S per chunk and warp
+    constexpr int kRows = kVRows / SPLIT;           // query rows per CTA
     constexpr int kDT = D / 8;                      // n-tiles of O
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* kring = smem;
@@ -103,17 +110,20 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
             L = a.max_seq_len;
         }
     }
-    const int rg = hh % a.head_groups;              // group of 64 rows of this KV head
+    const int rg = hh % a.head_groups;              // group of kRows rows of this KV head
     const int kvh = hh / a.head_groups;
     const int R = a.group;                          // rows of the KV head
-    const int rw = rg * kVRows + warp * 16;         // this warp's first row
+    const int half = SPLIT == 2 ? (warp & 1) : 0;   // which half of each chunk's positions (SPLIT 2)
+    const int tile = warp / SPLIT;                  // 16-row tile of this warp
+    const int pc0 = half * (kChunk / SPLIT);        // first chunk position of this warp
+    int rw = rg * kRows + tile * 16;                // this warp's first row
     const int ra = rw + g, rb = rw + g + 8;         // this lane's rows
     T* out = reinterpret_cast<T*>(a.out);
     const int bs = a.block_size;
     const int start = part * P;
 
     if (L <= 0) {                                   // empty sequence: zeros
-        if (part == 0 && warp < kVW)
+        if (part == 0 && warp < kVW && half == 0)
             for (int i = lane; i < 16 * D; i += 32) {
                 const int r = rw + i / D;
                 if (r < R) out[vrow_offset(a, s, kvh, r) * D + i % D] = T(0.0f);
@@ -184,7 +194,7 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
     // ================================================================ consumer warps
     // Q as the A operand (rows x head_dim), per 16-wide k-step: (row a, k 2t..2t+1),
     // (row b, same k), (row a, k 2t+8..2t+9), (row b, same k)
-    const bool va = ra < R, vb = rb < R;
+    bool va = ra < R, vb = rb < R;
     uint32_t qa[D / 16][4];
     {
         const uint32_t* qra = reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(a.q) +
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
 #pragma unroll
             for (int np = 0; np < kNT / 2; ++np) {
                 uint32_t bf[4];
-                const int pos = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int pos = pc0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
                 ldmatrix_x4(bf, dec::swz(kst + (ks >> 2) * G::kPlane, pos, (ks & 3) * 2 + ((lane >> 3) & 1)));
                 M::run(sacc[2 * np], qa[ks], bf[0], bf[1]);
                 M::run(sacc[2 * np + 1], qa[ks], bf[2], bf[3]);
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
         for (int j = 0; j < kNT; ++j) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int pc = 8 * j + 2 * t + e;    // position within the chunk
+                const int pc = pc0 + 8 * j + 2 * t + e;   // position within the chunk
                 const int pos = tok0 + pc;
                 sacc[j][e] = (pc < nv && pos < lim_a) ? sacc[j][e] * sl2 : -INFINITY;
                 sacc[j][2 + e] = (pc < nv && pos < lim_b) ? sacc[j][2 + e] * sl2 : -INFINITY;
@@ -308,19 +318,19 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
         }
         // ---- O += P V; V fragments by ldmatrix.trans, positions past the partition zeroed
         // in registers (a slot past the sequence may hold NaN, and 0 * NaN is NaN)
-        const bool tail = nv < kChunk;
+        const bool tail = nv < pc0 + kChunk / SPLIT;
 #pragma unroll
         for (int kk = 0; kk < kNT / 2; ++kk) {
             uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;   // keep-masks of positions 16kk+2t(+1), +8
             if (tail) {
-                const int p0 = 16 * kk + 2 * t;
+                const int p0 = pc0 + 16 * kk + 2 * t;
                 mlo = (p0 < nv ? 0x0000FFFFu : 0u) | (p0 + 1 < nv ? 0xFFFF0000u : 0u);
                 mhi = (p0 + 8 < nv ? 0x0000FFFFu : 0u) | (p0 + 9 < nv ? 0xFFFF0000u : 0u);
             }
 #pragma unroll
             for (int dp = 0; dp < kDT / 2; ++dp) {
                 uint32_t vf[4];
-                const int pos = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int pos = pc0 + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
                 const int dch = 2 * dp + (lane >> 4);   // 8-element column chunk over head_dim
                 ldmatrix_x4_trans(vf, dec::swz(vst + (dch >> 3) * G::kPlane, pos, dch & 7));
                 vf[0] &= mlo;
@@ -342,6 +352,49 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
     }
 
     if (threadIdx.x == 0) launch_dependents();      // the main loop is done: the next kernel may launch
+
+    // ---- SPLIT 2: the warp of the second half hands its state to the warp of
+    // the first (the same lane holds the same rows and columns), which merges
+    // it like two partitions; the ring is free once every warp is past its
+    // last chunk
+    if constexpr (SPLIT == 2) {
+        constexpr int kSlot = kDT * 4 + 4;          // floats per lane: o, then (m_a, m_b, l_a, l_b)
+        float* sc = reinterpret_cast<float*>(kring) + (tile * 32 + lane) * kSlot;
+        if (!epi_sync()) return;
+        if (half == 1) {
+#pragma unroll
+            for (int dn = 0; dn < kDT; ++dn)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[4 * dn + i] = o[dn][i];
+            sc[4 * kDT] = m_a;
+            sc[4 * kDT + 1] = m_b;
+            sc[4 * kDT + 2] = l_a;
+            sc[4 * kDT + 3] = l_b;
+        }
+        if (!epi_sync()) return;
+        if (half == 0) {
+            const float m2a = sc[4 * kDT], m2b = sc[4 * kDT + 1];
+            const float Ma = fmaxf(m_a, m2a), Mb = fmaxf(m_b, m2b);
+            // a row neither half saw keeps max -inf and zero state
+            const float w1a = Ma == -INFINITY ? 0.0f : fast_exp2(m_a - Ma);
+            const float w2a = Ma == -INFINITY ? 0.0f : fast_exp2(m2a - Ma);
+            const float w1b = Mb == -INFINITY ? 0.0f : fast_exp2(m_b - Mb);
+            const float w2b = Mb == -INFINITY ? 0.0f : fast_exp2(m2b - Mb);
+#pragma unroll
+            for (int dn = 0; dn < kDT; ++dn) {
+                o[dn][0] = o[dn][0] * w1a + sc[4 * dn] * w2a;
+                o[dn][1] = o[dn][1] * w1a + sc[4 * dn + 1] * w2a;
+                o[dn][2] = o[dn][2] * w1b + sc[4 * dn + 2] * w2b;
+                o[dn][3] = o[dn][3] * w1b + sc[4 * dn + 3] * w2b;
+            }
+            l_a = l_a * w1a + sc[4 * kDT + 2] * w2a;
+            l_b = l_b * w1b + sc[4 * kDT + 3] * w2b;
+            m_a = Ma;
+            m_b = Mb;
+        } else {
+            va = vb = false;                        // the first-half warp writes these rows
+        }
+    }
 
     // ================================================= epilogue: this warp's rows are complete
 #pragma unroll
@@ -389,7 +442,7 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
         if (tk == static_cast<unsigned>(nparts - 1)) *ticket = 0u;   // reset for the next run
     }
     if (!epi_sync()) return;
-    if (!*merge_flag) return;
+    if (!*merge_flag || half == 1) return;
     // last partition of this (sequence, row group): each warp merges its own rows;
     // lane covers head-dim elements [lane * D/32, +D/32)
     constexpr int kPer = D / 32;
@@ -426,7 +479,10 @@ template <typename T, int D>
 cudaError_t launch_verify_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
     constexpr size_t smem = VSmem<D>::kBytes;
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = verify_kernel<T, D>;
+    static_assert(2 * 32 * (D / 8 * 4 + 4) * sizeof(float) <= 2 * kVStages * Geo<D, kVW>::kStage,
+                  "the half-merge scratch fits the ring");
+    // up to 32 rows per KV head: two warps per 16-row tile (head_groups is 1 either way)
+    auto kern = a.group <= kVRows / 2 ? verify_kernel<T, D, 2> : verify_kernel<T, D, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
@@ -470,12 +526,13 @@ cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
 
 namespace pkv {
 
-int verify_ctas_per_sm(int head_dim) {
-    static int cache[2] = {-1, -1};
-    const int i = head_dim == 64 ? 0 : 1;
+int verify_ctas_per_sm(int head_dim, int rows) {
+    static int cache[4] = {-1, -1, -1, -1};
+    const bool split = rows <= kVRows / 2;
+    const int i = (head_dim == 64 ? 0 : 1) + (split ? 2 : 0);
     if (cache[i] < 0) {
         int n = 0;
-        const size_t smem = i == 0 ? VSmem<64>::kBytes : VSmem<128>::kBytes;
+        const size_t smem = head_dim == 64 ? VSmem<64>::kBytes : VSmem<128>::kBytes;
         auto set_and_query = [&](auto kern) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
                     cudaSuccess &&
@@ -483,7 +540,12 @@ int verify_ctas_per_sm(int head_dim) {
                 return n;
             return 0;
         };
-        cache[i] = i == 0 ? set_and_query(verify_kernel<__half, 64>) : set_and_query(verify_kernel<__half, 128>);
+        switch (i) {
+            case 0: cache[i] = set_and_query(verify_kernel<__half, 64, 1>); break;
+            case 1: cache[i] = set_and_query(verify_kernel<__half, 128, 1>); break;
+            case 2: cache[i] = set_and_query(verify_kernel<__half, 64, 2>); break;
+            default: cache[i] = set_and_query(verify_kernel<__half, 128, 2>); break;
+        }
     }
     return cache[i];
 }

@@ -3,7 +3,8 @@
 The last num_queries positions of each sequence are the query tokens' own K/V;
 query token i sees positions < L - num_queries + i + 1.  Cases cover query
 rows that fit one 8-row group and several, more than 16 rows per KV head (the
-rows-as-M kernel, one and two 64-row groups, partly filled warps), one and
+rows-as-M kernel: up to 32 rows with two warps per 16-row tile, one and two
+64-row groups, partly filled warps), with and without the lengths' sum, one and
 several partitions, query tokens that see nothing in a late partition, an
 empty sequence, both head sizes and every block size.
 """
@@ -40,12 +41,16 @@ CASES = [
     dict(num_heads=16, num_kv_heads=2, head_dim=128, block_size=32, dtype=W.F16, nq=8, lens=("fixed", (8, 900, 77))),
     dict(num_heads=8, num_kv_heads=1, head_dim=64, block_size=8, dtype=W.BF16, nq=10, lens=("fixed", (10, 400, 1025))),
     dict(num_heads=64, num_kv_heads=8, head_dim=128, block_size=16, dtype=W.F16, nq=3, lens=("fixed", (0, 3, 2049, 700))),
+    # exactly 32 rows per KV head at head_dim 64: two warps share each 16-row tile
+    dict(num_heads=16, num_kv_heads=2, head_dim=64, block_size=16, dtype=W.BF16, nq=4,
+         lens=("fixed", (4, 31, 33, 95, 97, 2100))),
 ]
 
 
+@pytest.mark.parametrize("with_sum", [False, True])
 @pytest.mark.parametrize("partition_tokens", [0, 64, 1024])
 @pytest.mark.parametrize("case", range(len(CASES)))
-def test_verify_matches_oracle(case, partition_tokens):
+def test_verify_matches_oracle(case, partition_tokens, with_sum):
     kw = dict(CASES[case])
     nq = kw.pop("nq")
     kw["num_seqs"] = len(kw["lens"][1])
@@ -58,7 +63,8 @@ def test_verify_matches_oracle(case, partition_tokens):
     qd = to_dev(q, s.dtype)
     out = torch.full_like(qd, float("nan"))
     pkv.paged_attention_verify(out, qd, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
-                               max_seq_len=wl.max_seq_len, partition_tokens=partition_tokens)
+                               max_seq_len=wl.max_seq_len, partition_tokens=partition_tokens,
+                               sum_seq_lens=int(wl.seq_lens.sum()) if with_sum else 0)
     torch.cuda.synchronize()
     kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
     ref = oracle.verify_attention_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
