@@ -252,34 +252,29 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
             put = pb >= 0 && nslot == static_cast<int64_t>(pb) * bs + (L - 1) % bs;
             if (!put && lane == 0) raise_error(a.err, kErrBounds);
         }
-        if (*abort_flag) return;
-        if (lane == 0) {
+        // Each storing lane orders its stores before the tile loads (async
+        // proxy) that lane 0 issues after the warp barrier.
+        if (put && lane < 2 * kHV) {
+            const int64_t at = (nslot * a.num_kv_heads + kvh) * kHV + lane % kHV;
+            if constexpr (KV8)
+                reinterpret_cast<uint2*>(lane < kHV ? a.key_cache : a.value_cache)[at] =
+                    quantize8<std::is_same<T, __nv_bfloat16>::value>(nrow, nscale);
+            else
+                reinterpret_cast<uint4*>(lane < kHV ? a.key_cache : a.value_cache)[at] = nrow;
+            fence_proxy_async_global();
+        }
+        __syncwarp();
+        if (lane == 0 && !*abort_flag) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-        }
-        const int per_chunk = kChunk / bs;
-        for (int c = 0; c < nchunks; ++c) {
-            const int st = c % STAGES;
-            const unsigned ph = (c / STAGES) & 1;
-            if (put && c == nchunks - 1) {          // the chunk holding position L - 1
-                if (lane < 2 * kHV) {
-                    const int64_t at = (nslot * a.num_kv_heads + kvh) * kHV + lane % kHV;
-                    if constexpr (KV8)
-                        reinterpret_cast<uint2*>(lane < kHV ? a.key_cache : a.value_cache)[at] =
-                            quantize8<std::is_same<T, __nv_bfloat16>::value>(nrow, nscale);
-                    else
-                        reinterpret_cast<uint4*>(lane < kHV ? a.key_cache : a.value_cache)[at] = nrow;
+            const int per_chunk = kChunk / bs;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c % STAGES;
+                const unsigned ph = (c / STAGES) & 1;
+                if (!dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
+                    dec::raise_abort(a.err, abort_flag);
+                    break;
                 }
-                fence_proxy_async_global();         // the tile loads below see these bytes
-                __syncwarp();
-            }
-            bool got = dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag);
-            got = __all_sync(0xffffffffu, got);
-            if (!got) {
-                if (lane == 0) dec::raise_abort(a.err, abort_flag);
-                break;
-            }
-            if (lane == 0) {
                 const int tok0 = start + c * kChunk;
                 const int nb = (min(end, tok0 + kChunk) - tok0 + bs - 1) / bs;
                 mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * kEB * 2));
@@ -293,7 +288,6 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
                     }
                 }
             }
-            __syncwarp();
         }
         return;
     }
