@@ -21,6 +21,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -55,6 +56,8 @@ def parse_args():
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
     p.add_argument("--ref-seconds", type=float, default=90.0, help="total budget of the --impl reference run")
+    p.add_argument("--layers", type=int, default=0,
+                   help="run a multi-layer workload with this many layers (same per-layer shape; 0 = all)")
     p.add_argument("--separate-append", action="store_true",
                    help="launch paged_kv_append and the decode separately instead of the fused call")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -250,6 +253,8 @@ def run_pkv(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     spec = W.SPECS[args.workload]
+    if args.layers and spec.num_layers > 1:
+        spec = dataclasses.replace(spec, num_layers=min(args.layers, spec.num_layers))
     wl = W.build(spec, values="none")
     tdt = torch.float16 if spec.dtype == W.F16 else torch.bfloat16
     nbytes = algorithmic_bytes(wl)
