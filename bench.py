@@ -64,6 +64,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--e2e-eager", action="store_true",
+                   help="end-to-end loop issues every call from Python instead of replaying a CUDA graph of the step")
     return p.parse_args()
 
 
@@ -392,16 +394,45 @@ def run_pkv(args, rank, world, local):
         def read_result(buf):                        # the host uses the step's result
             return float(buf[0].view(-1)[0].float()) + float(buf[-1].view(-1)[-1].float())
 
-        torch.cuda.synchronize()
-        barrier(world)
-        w0 = time.perf_counter()
-        for i in range(n_e2e):
-            j = i % 2
+        def whole_step(i, j):                    # inputs in, the step, outputs out
             for h, d_ in zip(host_in, dev_in):
                 d_.copy_(h, non_blocking=True)
             step(i, False)
             for h, o in zip(host_out[j], outs):
                 h.copy_(o, non_blocking=True)
+
+        graphs = None
+        if not args.e2e_eager:
+            # one CUDA graph per (pool replica, output buffer), captured through the same
+            # public calls; a replay copies the inputs in, plans, decodes and copies the
+            # outputs back, with one launch from the host
+            torch.cuda.synchronize()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for r in range(replicas):
+                    whole_step(r, 0)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graphs = {}
+            for r in range(replicas):
+                for j in range(2):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                        whole_step(r, j)
+                    graphs[(r, j)] = g
+            torch.cuda.synchronize()
+            assert pkv.device_error() == 0, "device error word raised while capturing"
+
+        torch.cuda.synchronize()
+        barrier(world)
+        w0 = time.perf_counter()
+        for i in range(n_e2e):
+            j = i % 2
+            if graphs is not None:
+                graphs[(i % replicas, j)].replay()
+            else:
+                whole_step(i, j)
             done[j].record()
             if i > 0:
                 done[1 - j].synchronize()
@@ -412,8 +443,10 @@ def run_pkv(args, rank, world, local):
         e2e = {"value": round(world * nbytes["step"] * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
                "ms_per_step": round(e2e_s * 1e3 / n_e2e, 4),
-               "pipeline": "every step copies its inputs in from pinned memory and its outputs back; the host "
-                           "reads step i's outputs while the GPU runs step i+1",
+               "pipeline": ("every step copies its inputs in from pinned memory and its outputs back; the host "
+                            "reads step i's outputs while the GPU runs step i+1; " +
+                            ("each step is one replay of a CUDA graph of the public calls"
+                             if graphs is not None else "every call issued from Python")),
                "finite": bool(math.isfinite(seen))}
 
     # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
