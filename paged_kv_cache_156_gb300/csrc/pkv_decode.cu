@@ -267,6 +267,9 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         if (lane == 0 && !*abort_flag) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
+            // K/V bytes are read once per step: evict them first, so the small data
+            // every CTA and layer reuses (tables, q, work items, partials) stays in L2
+            const uint64_t pol = l2_policy_evict_first();
             const int per_chunk = kChunk / bs;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % STAGES;
@@ -283,8 +286,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
 #pragma unroll
                     for (int hf = 0; hf < G::kHalves; ++hf) {
                         const int off = st * G::kStage + hf * G::kPlane + j * bs * 128;
-                        tma_load_4d(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st]);
-                        tma_load_4d(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st]);
+                        tma_load_4d_hint(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st], pol);
+                        tma_load_4d_hint(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st], pol);
                     }
                 }
             }

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
         if (lane == 0 && !*abort_flag) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
+            const uint64_t pol = l2_policy_evict_first();   // K/V read once: keep the reused data in L2
             const int per_chunk = kChunk / bs;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % kVStages;
@@ -182,8 +183,8 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
 #pragma unroll
                     for (int hf = 0; hf < G::kHalves; ++hf) {
                         const int off = st * G::kStage + hf * G::kPlane + j * bs * 128;
-                        tma_load_4d(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st]);
-                        tma_load_4d(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st]);
+                        tma_load_4d_hint(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st], pol);
+                        tma_load_4d_hint(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st], pol);
                     }
                 }
             }

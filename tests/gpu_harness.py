@@ -63,6 +63,22 @@ class DeviceStep:
             pkv.paged_kv_append(self.k_new, self.v_new, self.kc[l], self.vc[l], self.slot_mapping)
             self.decode(l)
 
+    def run_planned_fused(self):
+        """The benchmark's step: copy-on-write copies, one plan for the step, then per layer
+        the slot write fused into the decode launch (one new token per sequence)."""
+        wl, s = self.wl, self.wl.spec
+        assert wl.num_tokens == s.num_seqs, "the fused call writes one token per sequence"
+        if self.copy_pairs.shape[0]:
+            pkv.copy_blocks(self.kc, self.vc, self.copy_pairs)
+        total = int(wl.seq_lens.sum())
+        pkv.decode_plan(self.workspace, self.block_tables, self.seq_lens, s.num_heads, self.kc[0], wl.max_seq_len,
+                        self.partition_tokens, sum_seq_lens=total)
+        for l in range(len(self.kc)):
+            pkv.paged_kv_append_decode(self.out[l], self.q, self.k_new, self.v_new, self.kc[l], self.vc[l],
+                                       self.slot_mapping, self.block_tables, self.seq_lens, wl.scale,
+                                       max_seq_len=wl.max_seq_len, workspace=self.workspace,
+                                       partition_tokens=self.partition_tokens, planned=True, sum_seq_lens=total)
+
     def decode(self, l=0):
         wl = self.wl
         pkv.paged_attention_decode(self.out[l], self.q, self.kc[l], self.vc[l], self.block_tables, self.seq_lens,

@@ -187,12 +187,17 @@ def test_lengths_above_max_seq_len_are_clamped_and_flagged(num_seqs):
 FULL = ["llama3_8b", "llama2_70b_mixed_bs16", "llama2_70b_mixed_bs32", "cow_fork", "cow_fork_partial"]
 
 
+@pytest.mark.parametrize("mode", ["separate", "fused"])
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_workload(name):
+def test_full_size_workload(name, mode):
+    """separate: append then decode calls; fused: the benchmark's launches (one plan with the
+    lengths' sum, then the fused slot write + decode over it)."""
     wl = W.build(W.SPECS[name], values="none")
+    if mode == "fused" and wl.num_tokens != wl.spec.num_seqs:
+        pytest.skip("this step writes several slots per sequence: the benchmark launches the append")
     step = DeviceStep(wl, pools="device")
     pre_k, pre_v = to_bits(step.kc[0]), to_bits(step.vc[0])
-    step.run()
+    step.run() if mode == "separate" else step.run_planned_fused()
     torch.cuda.synchronize()
     s = wl.spec
     part = pkv.decode_plan_partition_tokens(step.workspace, s.num_seqs, s.num_heads, s.num_kv_heads)
@@ -208,12 +213,13 @@ def test_full_size_workload(name):
     assert err <= TOL[wl.spec.dtype], f"{name}: max abs err {err} on sequences {seqs}"
 
 
-def test_full_size_80_layer_step():
+@pytest.mark.parametrize("mode", ["separate", "fused"])
+def test_full_size_80_layer_step(mode):
     wl = W.build(W.SPECS["llama2_70b_step"], values="none")
     step = DeviceStep(wl, pools="device")
     check_layers = (0, 41, 79)
     pre = {l: (to_bits(step.kc[l]), to_bits(step.vc[l])) for l in check_layers}
-    step.run()
+    step.run() if mode == "separate" else step.run_planned_fused()
     torch.cuda.synchronize()
     for l in range(80):
         assert torch.isfinite(step.out[l]).all(), f"layer {l}"
