@@ -18,8 +18,14 @@
 //  * The CTA's slice of the block table is staged in shared memory once; a
 //    producer warp then streams the partition's K and V tiles with TMA
 //    (cp.async.bulk.tensor; one box = one (physical block, KV head) tile of
-//    block_size rows x 64 elements, 128B-swizzled) into a ring of STAGES
-//    chunks of 64 positions, handing each chunk over with an mbarrier.
+//    block_size rows x 64 elements, 128B-swizzled, loaded with an L2
+//    evict-first policy: K/V bytes are read once per step) into a ring of
+//    STAGES chunks of 64 positions, handing each chunk over with an mbarrier.
+//  * With the step's slot write fused in (pkv_paged_kv_append_decode), the
+//    producer warp of the CTA that holds position seq_len - 1 first stores
+//    the sequence's new K and V rows for its KV head into that slot (after
+//    checking the slot against the table) and fences them against its own
+//    tile loads ("LLM 推理引擎内部原理" §2.3: append_slot gives the slot).
 //  * Four consumer warps each own 16 positions of every chunk.  Scores are a
 //    small dense contraction over the query-head group, done on the tensor
 //    cores with keys as the M dimension: S^T[16 pos x 8 heads] = K Q^T

@@ -225,3 +225,27 @@ def test_fused_host_validation():
         pkv.paged_kv_append_decode(out, x.q, x.k[:-1], x.v[:-1], kc, vc, x.slots[:-1], x.tables, x.lens)
     with pytest.raises(ValueError):                 # slots are int64
         pkv.paged_kv_append_decode(out, x.q, x.k, x.v, kc, vc, x.slots.int(), x.tables, x.lens)
+
+
+def test_fused_above_plan_limit_full_grid():
+    """More sequences than the plan lists (the decode runs its full 3-D grid): the fused write
+    is made by the CTA of the last partition, as with a plan."""
+    B = pkv.PLAN_MAX_SEQS + 76
+    rng = np.random.default_rng(790)
+    lens = rng.integers(1, 700, B)
+    lens[rng.random(B) < 0.05] = 0
+    wl = W.build(W.small_spec(num_seqs=B, num_heads=16, num_kv_heads=4, head_dim=128, block_size=16, dtype=W.F16,
+                              seed=791, lens=("fixed", tuple(int(x) for x in lens)), pool=("headroom", 0.1)))
+    s = wl.spec
+    x = Inputs(wl)
+    kc, vc = device_pools(wl)
+    out = fused(wl, x, kc, vc, 256, False, None)
+    torch.cuda.synchronize()
+    rk, rv = wl.key_caches[0].copy(), wl.value_caches[0].copy()
+    oracle.append_ref(rk, rv, wl.k_new, wl.v_new, wl.slot_mapping)
+    assert np.array_equal(pool_bits(kc), rk) and np.array_equal(pool_bits(vc), rv)
+    seqs = np.random.default_rng(792).choice(B, 40, replace=False)
+    ref = oracle.attention_ref(wl.q[seqs], rk, rv, wl.block_tables[seqs], wl.seq_lens[seqs], wl.scale,
+                               s.num_kv_heads, s.dtype)
+    assert torch.isfinite(out).all()
+    assert max_abs_err(out, ref, seqs) <= TOL[s.dtype]
