@@ -347,9 +347,9 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.qgroup = num_heads / num_kv_heads;
     a.num_queries = num_queries;
     a.group = a.qgroup * num_queries;
-    // more than kVerifyMinRows query rows per KV head: the verify kernel, 64 rows per CTA
+    // more than kVerifyMinRows query rows per KV head: the verify kernel, 32 or 64 rows per CTA
     const bool verify_kernel = num_queries > 1 && a.group > pkv::kVerifyMinRows;
-    a.head_groups = verify_kernel ? (a.group + pkv::kVerifyRowsPerCta - 1) / pkv::kVerifyRowsPerCta
+    a.head_groups = verify_kernel ? (a.group + pkv::verify_rows_per_cta(a.group) - 1) / pkv::verify_rows_per_cta(a.group)
                                   : (a.group + 7) / 8;
     a.block_size = block_size;
     a.part_tokens = part;

@@ -482,8 +482,8 @@ cudaError_t launch_verify_t(const DecodeArgs& a, const CUtensorMap& tmk, const C
     static_assert(smem <= 232448, "shared memory budget");
     static_assert(2 * 32 * (D / 8 * 4 + 4) * sizeof(float) <= 2 * kVStages * Geo<D, kVW>::kStage,
                   "the half-merge scratch fits the ring");
-    // up to 32 rows per KV head: two warps per 16-row tile (head_groups is 1 either way)
-    auto kern = a.group <= kVRows / 2 ? verify_kernel<T, D, 2> : verify_kernel<T, D, 1>;
+    // 32 rows per CTA: two warps per 16-row tile; 64: one warp per tile (head_groups matches)
+    auto kern = verify_rows_per_cta(a.group) == kVRows / 2 ? verify_kernel<T, D, 2> : verify_kernel<T, D, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
@@ -527,9 +527,18 @@ cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
 
 namespace pkv {
 
+int verify_rows_per_cta(int rows) {
+    static const int forced = [] {
+        const char* e = getenv("PKV_VERIFY_ROWS");       // tuning knob: 32 or 64 rows per CTA
+        return e ? atoi(e) : 0;
+    }();
+    if (rows <= kVRows / 2) return kVRows / 2;
+    return forced == kVRows / 2 ? kVRows / 2 : kVRows;
+}
+
 int verify_ctas_per_sm(int head_dim, int rows) {
     static int cache[4] = {-1, -1, -1, -1};
-    const bool split = rows <= kVRows / 2;
+    const bool split = verify_rows_per_cta(rows) == kVRows / 2;
     const int i = (head_dim == 64 ? 0 : 1) + (split ? 2 : 0);
     if (cache[i] < 0) {
         int n = 0;
