@@ -362,7 +362,20 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     // could need, or, with the lengths' sum known, at most B + sum / P entries (a sequence
     // of length l has max(1, ceil(l / P)) <= 1 + l / P partitions)
     int64_t capacity = static_cast<int64_t>(num_seqs) * max_parts;
-    if (sum_seq_lens > 0) capacity = std::min(capacity, static_cast<int64_t>(num_seqs) + sum_seq_lens / part);
+    if (sum_seq_lens > 0) {
+        capacity = std::min(capacity, static_cast<int64_t>(num_seqs) + sum_seq_lens / part);
+        if (partition_tokens == 0) {
+            // The plan's automatic size is never below pb = min(max(rule size, part), table
+            // span) unless every sequence fits one partition; later adjustments only lower the
+            // item count.  So at most B + sum / pb items, and B when no length exceeds pb.
+            const int64_t nh = static_cast<int64_t>(a.num_kv_heads) * a.head_groups;
+            const int64_t rule = pkv::plan_rule_tokens(sum_seq_lens, nh, kv8, a.slots > 0 ? a.slots : 1);
+            const int64_t pb = std::min<int64_t>(std::max<int64_t>(rule, part),
+                                                 static_cast<int64_t>(pkv::kPlanTableEntries) * block_size);
+            const int64_t bound = static_cast<int64_t>(num_seqs) + (max_seq_len > pb ? sum_seq_lens / pb : 0);
+            capacity = std::min(capacity, bound);
+        }
+    }
     a.plan_capacity = static_cast<int>(capacity);
     a.sum_seq_lens = sum_seq_lens;
     a.scale_log2 = scale * 1.4426950408889634f;

@@ -12,7 +12,7 @@
 namespace pkv {
 namespace dec {
 
-constexpr int kMaxTable = 512;       // staged table entries: part_tokens (<= 4096) / block_size (>= 8)
+constexpr int kMaxTable = kPlanTableEntries;   // staged table entries: part_tokens (<= 4096) / block_size (>= 8)
 constexpr int kHeadsPerCta = 8;      // mma N: query heads served by one CTA
 constexpr int kMaxParts = 512;       // partitions per sequence the in-kernel merge handles
 

@@ -46,7 +46,7 @@ namespace {
 
 constexpr int kRankSeqs = 64;                       // sequences each CTA ranks and writes
 constexpr int kMaxWarps = kPlanMaxSeqs / 32;
-constexpr int kGranule = 512;                       // automatic partition sizes: multiples of 512 positions
+constexpr int kGranule = kPlanGranule;              // automatic partition sizes: multiples of 512 positions
 
 template <typename V>
 __device__ __forceinline__ V warp_sum(V v) {
@@ -147,9 +147,7 @@ __global__ void __launch_bounds__(kPlanMaxSeqs) plan_kernel(const DecodeArgs a) 
     if (a.part_auto) {
         // 0.85 x the positions per slot, counted in 16-bit-pool bytes: an E4M3
         // position is half the bytes, so its partitions are twice as long
-        const long long target = (W * nh * (a.kv8 ? 34 : 17)) / (slots * 20);
-        long long p = ((target + kGranule / 2) / kGranule) * kGranule;       // nearest multiple of 512
-        p = max(p, static_cast<long long>(kGranule));
+        const long long p = plan_rule_tokens(W, nh, a.kv8 != 0, slots);
         const int table_cap = dec::kMaxTable * a.block_size;
         cap = max(a.part_tokens, min(table_cap, (lmax + 63) / 64 * 64));
         P0 = static_cast<int>(min(max(p, static_cast<long long>(a.part_tokens)), static_cast<long long>(cap)));

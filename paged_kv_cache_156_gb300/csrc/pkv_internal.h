@@ -106,6 +106,22 @@ struct DecodeArgs {
 // direct grid (one CTA per (KV head group, partition, sequence)).
 constexpr int kPlanMaxSeqs = 1024;
 
+// Block-table entries a decode CTA stages (a partition spans at most this many blocks).
+constexpr int kPlanTableEntries = 512;
+// Automatic partition sizes are multiples of this many positions.
+constexpr int kPlanGranule = 512;
+
+// The plan kernel's automatic partition size from the lengths' sum alone:
+// about 0.85 x the positions per resident CTA slot (sum * nh / slots), counted
+// in 16-bit-pool bytes (an E4M3 position is half the bytes, so twice as many),
+// rounded to the nearest multiple of kPlanGranule, at least one granule.  The
+// host uses the same rule to bound the work list the grid must cover.
+__host__ __device__ inline long long plan_rule_tokens(long long sum_lens, long long nh, bool kv8, long long slots) {
+    const long long target = (sum_lens * nh * (kv8 ? 34 : 17)) / (slots * 20);
+    const long long p = ((target + kPlanGranule / 2) / kPlanGranule) * kPlanGranule;
+    return p > kPlanGranule ? p : kPlanGranule;
+}
+
 // Workspace layout of one decode call:
 //   [tickets | work list | partial outputs | (max, sum) pairs]
 // each region 256-byte aligned.  Every call re-initialises what it uses.
