@@ -11,8 +11,8 @@
 //
 //  * partition size: at least the host's choice; when the call asks for the
 //    automatic size, about 0.85 x the positions per resident CTA slot
-//    (sum_s L_s * KV head groups / slots; twice that for an E4M3 pool, whose
-//    positions are half the bytes), in multiples of 512, capped by the
+//    (sum_s L_s * KV head groups / slots; 1.4 times that for an E4M3 pool,
+//    whose positions are half the bytes), in multiples of 512, capped by the
 //    longest sequence and by the staged table, raised when the item count
 //    would spill a quarter wave or less past one full wave, then shrunk to
 //    the smallest multiple of 64 that splits the longest sequence into as
@@ -145,8 +145,7 @@ __global__ void __launch_bounds__(kPlanMaxSeqs) plan_kernel(const DecodeArgs a) 
     int P0 = a.part_tokens, q0 = a.part_tokens;
     int cap = a.part_tokens;
     if (a.part_auto) {
-        // 0.85 x the positions per slot, counted in 16-bit-pool bytes: an E4M3
-        // position is half the bytes, so its partitions are twice as long
+        // 0.85 x the positions per slot (an E4M3 position counts 1.4 times)
         const long long p = plan_rule_tokens(W, nh, a.kv8 != 0, slots);
         const int table_cap = dec::kMaxTable * a.block_size;
         cap = max(a.part_tokens, min(table_cap, (lmax + 63) / 64 * 64));
