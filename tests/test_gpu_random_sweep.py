@@ -1,4 +1,5 @@
-"""Randomized GPU parity sweep: seeded random batches against the oracle.
+"""Randomized GPU parity sweep: seeded random batches against the oracle, through the
+separate calls and through one plan plus the fused slot write + decode.
 
 Each case draws a shape (heads, KV heads, head size, block size, dtype), a
 batch (sequence count, length distribution with ragged tails and empty
@@ -79,6 +80,45 @@ def test_random_batch_matches_oracle(seed):
         kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
         assert np.array_equal(to_bits(step.kc[0]), kc) and np.array_equal(to_bits(step.vc[0]), vc)
         ref = oracle.attention_ref(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
+    assert torch.isfinite(out).all()
+    err = max_abs_err(out, ref)
+    assert err <= TOL[s.dtype], f"case {seed} ({s}, partition {part}): max abs err {err}"
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batch_fused_planned(seed):
+    """The same random batches through the benchmark's launches: one plan with the lengths'
+    sum, then the slot write fused into the decode (16-bit or E4M3 pools)."""
+    spec, part = draw_case(seed)
+    wl = W.build(spec)
+    s = wl.spec
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    q, k, v = to_dev(wl.q, s.dtype), to_dev(wl.k_new, s.dtype), to_dev(wl.v_new, s.dtype)
+    tables, lens, slots = dev(wl.block_tables), dev(wl.seq_lens), dev(wl.slot_mapping)
+    if s.fp8:
+        kc, vc = dev(wl.key_caches[0]), dev(wl.value_caches[0])
+        ks, vs = dev(wl.k_scales[0]), dev(wl.v_scales[0])
+    else:
+        kc, vc = to_dev(wl.key_caches[0], s.dtype), to_dev(wl.value_caches[0], s.dtype)
+        ks = vs = None
+    total = int(wl.seq_lens.sum())
+    ws = pkv.alloc_workspace(s.num_seqs, s.num_heads, s.num_kv_heads, s.head_dim, wl.max_seq_len, part)
+    pkv.decode_plan(ws, tables, lens, s.num_heads, kc, wl.max_seq_len, part, sum_seq_lens=total)
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_kv_append_decode(out, q, k, v, kc, vc, slots, tables, lens, wl.scale, max_seq_len=wl.max_seq_len,
+                               workspace=ws, partition_tokens=part, planned=True, sum_seq_lens=total, k_scale=ks,
+                               v_scale=vs)
+    torch.cuda.synchronize()
+    rk, rv = wl.key_caches[0].copy(), wl.value_caches[0].copy()
+    if s.fp8:
+        oracle.append_fp8_ref(rk, rv, wl.k_new, wl.v_new, wl.slot_mapping, wl.k_scales[0], wl.v_scales[0], s.dtype)
+        assert np.array_equal(kc.cpu().numpy(), rk) and np.array_equal(vc.cpu().numpy(), rv)
+        ref = oracle.attention_fp8_ref(wl.q, rk, rv, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype,
+                                       wl.k_scales[0], wl.v_scales[0])
+    else:
+        oracle.append_ref(rk, rv, wl.k_new, wl.v_new, wl.slot_mapping)
+        assert np.array_equal(to_bits(kc), rk) and np.array_equal(to_bits(vc), rv)
+        ref = oracle.attention_ref(wl.q, rk, rv, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
     assert torch.isfinite(out).all()
     err = max_abs_err(out, ref)
     assert err <= TOL[s.dtype], f"case {seed} ({s}, partition {part}): max abs err {err}"
