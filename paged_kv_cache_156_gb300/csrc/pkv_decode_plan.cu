@@ -97,22 +97,26 @@ __global__ void __launch_bounds__(kPlanMaxSeqs) plan_kernel(const DecodeArgs a) 
     launch_dependents();                            // the decode grid may launch now; it waits for this grid
 
     // ---- this thread's sequence and its predecessor (for the prefix-group test):
-    // length clamped to [0, max_seq_len], first physical block (-1: empty)
-    auto first_block = [&](int s, int L) {
-        return (L > 0 && a.max_blocks_per_seq > 0) ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq)
-                                                   : -1;
+    // length clamped to [0, max_seq_len], first physical block (-1: empty).  The
+    // lengths and the first table entries are loaded together (one round trip);
+    // an entry counts only for a non-empty sequence.
+    auto first_entry = [&](int s) {
+        return a.max_blocks_per_seq > 0 ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq) : -1;
     };
     int L = 0, b0 = -1, bp = -1;
     if (t < B) {
         L = __ldg(a.seq_lens + t);
-        const int Lp = t > 0 ? min(max(__ldg(a.seq_lens + t - 1), 0), a.max_seq_len) : 0;
+        const int Lp_raw = t > 0 ? __ldg(a.seq_lens + t - 1) : 0;
+        const int e0 = first_entry(t);
+        const int ep = t > 0 ? first_entry(t - 1) : -1;
+        const int Lp = min(max(Lp_raw, 0), a.max_seq_len);
         if (L > a.max_seq_len) {                    // precondition broken: attend over max_seq_len
             if (blockIdx.x == 0) raise_error(a.err, kErrBounds);
             L = a.max_seq_len;
         }
         L = max(L, 0);
-        b0 = first_block(t, L);
-        bp = t > 0 ? first_block(t - 1, Lp) : -1;
+        b0 = L > 0 ? e0 : -1;
+        bp = Lp > 0 ? ep : -1;
         sGmax[t] = 0;
     }
     // a group starts at a sequence that does not continue its predecessor's first block
