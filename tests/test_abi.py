@@ -79,6 +79,30 @@ def test_validation_rejects_before_launch(lib):
     assert lib.pkv_copy_blocks(None, None, 0, null, 0, 4, 16, 2, 64, 0, null) == pkv.PKV_OK
 
 
+def test_fused_and_verify_validation_rejects_before_launch(lib):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(256)            # a non-null, aligned address that nothing dereferences
+
+    def fused(head_dim=128, dt=0, kv_dt=0, k_scale=null, v_scale=null, sum_lens=0, ptr=fake, slots=fake):
+        # out, q, k, v, key_cache, value_cache, slot_mapping, tables, width, lens, B, max_len, sum, Hq, Hkv, d, bs,
+        # num_blocks, scale, dt, kv_dt, k_scale, v_scale, workspace, workspace_bytes, partition, planned, stream
+        return lib.pkv_paged_kv_append_decode(ptr, ptr, ptr, ptr, ptr, ptr, slots, fake, 4, fake, 2, 10, sum_lens, 8, 2,
+                                              head_dim, 16, 10, 1.0, dt, kv_dt, k_scale, v_scale, null, 0, 0, 1, null)
+
+    assert fused(sum_lens=-1) == pkv.PKV_ERR_INVALID
+    assert fused(kv_dt=1) == pkv.PKV_ERR_INVALID and b"kv_dt" in lib.pkv_last_error()   # 16-bit pools: kv_dt == dt
+    assert fused(kv_dt=2) == pkv.PKV_ERR_INVALID                                          # E4M3 without scales
+    assert fused(head_dim=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert fused(head_dim=64, kv_dt=2, k_scale=fake, v_scale=fake) == pkv.PKV_ERR_UNSUPPORTED   # E4M3: head_dim 128
+    assert fused(ptr=null) == pkv.PKV_ERR_INVALID and b"null" in lib.pkv_last_error()
+    assert fused(slots=null) == pkv.PKV_ERR_INVALID and b"null" in lib.pkv_last_error()
+    assert fused(slots=ctypes.c_void_p(260)) == pkv.PKV_ERR_INVALID                      # slot_mapping 8-byte aligned
+    # verify: a negative lengths' sum is refused
+    st = lib.pkv_paged_attention_verify(fake, fake, fake, fake, fake, 4, fake, 2, 10, -1, 8, 2, 128, 16, 10, 1.0, 0, 4,
+                                        null, 0, 0, null)
+    assert st == pkv.PKV_ERR_INVALID
+
+
 def test_workspace_formula(lib):
     # explicit partition sizes need no device query
     B, Hq, Hkv, d = 16, 64, 8, 128
