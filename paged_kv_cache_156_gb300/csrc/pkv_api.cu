@@ -6,10 +6,13 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/pkv.h"
 #include "pkv_internal.h"
@@ -37,6 +40,24 @@ pkv_status ok() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An NVTX range around each launching call when PKV_NVTX is set in the
+// environment: a profiler's timeline then shows which call issued which kernels.
+bool nvtx_enabled() {
+    static const bool v = getenv("PKV_NVTX") != nullptr;
+    return v;
+}
+struct CallRange {
+    bool on;
+    explicit CallRange(const char* name) : on(nvtx_enabled()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~CallRange() {
+        if (on) nvtxRangePop();
+    }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -186,6 +207,7 @@ const char* pkv_last_error(void) { return g_msg; }
 pkv_status pkv_paged_kv_append(const void* k, const void* v, void* key_cache, void* value_cache,
                                const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
                                int block_size, int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    CallRange range_("pkv_paged_kv_append");
     if (num_tokens < 0) return fail(PKV_ERR_INVALID, "num_tokens %lld < 0", static_cast<long long>(num_tokens));
     if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
     if (num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0)
@@ -406,6 +428,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* key_
                                       int num_seqs, int max_seq_len, int num_heads, int num_kv_heads, int head_dim,
                                       int block_size, int64_t num_blocks, float scale, pkv_dtype dt, void* workspace,
                                       size_t workspace_bytes, int partition_tokens, void* stream) {
+    CallRange range_("pkv_paged_attention_decode");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
                           workspace, workspace_bytes, partition_tokens, stream);
@@ -417,6 +440,7 @@ pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_
                                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
                                       pkv_dtype dt, int num_queries, void* workspace, size_t workspace_bytes,
                                       int partition_tokens, void* stream) {
+    CallRange range_("pkv_paged_attention_verify");
     if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt,
@@ -428,6 +452,7 @@ pkv_status pkv_decode_plan(const int32_t* block_tables, int max_blocks_per_seq, 
                            int max_seq_len, int64_t sum_seq_lens, int num_heads, int num_kv_heads, int head_dim,
                            int block_size, pkv_dtype kv_dt, void* workspace, size_t workspace_bytes,
                            int partition_tokens, void* stream) {
+    CallRange range_("pkv_decode_plan");
     if (!valid_dtype(kv_dt) && kv_dt != PKV_E4M3) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(kv_dt));
     if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(nullptr, nullptr, nullptr, nullptr, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
@@ -443,6 +468,7 @@ pkv_status pkv_paged_attention_decode_planned(void* out, const void* q, const vo
                                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                               float scale, pkv_dtype dt, void* workspace, size_t workspace_bytes,
                                               int partition_tokens, void* stream) {
+    CallRange range_("pkv_paged_attention_decode_planned");
     if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
@@ -458,6 +484,7 @@ pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void* q, cons
                                                   int64_t num_blocks, float scale, pkv_dtype dt,
                                                   const float* k_scale, const float* v_scale, void* workspace,
                                                   size_t workspace_bytes, int partition_tokens, void* stream) {
+    CallRange range_("pkv_paged_attention_decode_fp8_planned");
     if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "k_scale / v_scale are required");
     if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
@@ -472,6 +499,7 @@ pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* 
                                           int block_size, int64_t num_blocks, float scale, pkv_dtype dt,
                                           const float* k_scale, const float* v_scale, void* workspace,
                                           size_t workspace_bytes, int partition_tokens, void* stream) {
+    CallRange range_("pkv_paged_attention_decode_fp8");
     if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "k_scale / v_scale are required");
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
@@ -485,6 +513,7 @@ pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const void* k, c
                                       int block_size, int64_t num_blocks, float scale, pkv_dtype dt, pkv_dtype kv_dt,
                                       const float* k_scale, const float* v_scale, void* workspace,
                                       size_t workspace_bytes, int partition_tokens, int planned, void* stream) {
+    CallRange range_("pkv_paged_kv_append_decode");
     if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
     if (kv_dt == PKV_E4M3) {
         if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "E4M3 pools need k_scale and v_scale");
@@ -505,6 +534,7 @@ pkv_status pkv_paged_kv_append_fp8(const void* k, const void* v, void* key_cache
                                    const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks, int block_size,
                                    int num_kv_heads, int head_dim, pkv_dtype dt, const float* k_scale,
                                    const float* v_scale, void* stream) {
+    CallRange range_("pkv_paged_kv_append_fp8");
     if (num_tokens < 0) return fail(PKV_ERR_INVALID, "num_tokens %lld < 0", static_cast<long long>(num_tokens));
     if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d (fp16 or bf16 inputs)", static_cast<int>(dt));
     if (num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0)
@@ -595,6 +625,7 @@ extern "C" {
 pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                            const int64_t* src_dst_pairs, int64_t num_pairs, int64_t num_blocks, int block_size,
                            int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    CallRange range_("pkv_copy_blocks");
     return block_copies(key_caches, value_caches, key_caches, value_caches, num_layers, src_dst_pairs, num_pairs,
                         num_blocks, num_blocks, block_size, num_kv_heads, head_dim, dt, stream, "copy_blocks");
 }
@@ -603,6 +634,7 @@ pkv_status pkv_swap_blocks(void* const* src_key_caches, void* const* src_value_c
                            void* const* dst_value_caches, int num_layers, const int64_t* src_dst_pairs,
                            int64_t num_pairs, int64_t src_num_blocks, int64_t dst_num_blocks, int block_size,
                            int num_kv_heads, int head_dim, pkv_dtype dt, void* stream) {
+    CallRange range_("pkv_swap_blocks");
     return block_copies(src_key_caches, src_value_caches, dst_key_caches, dst_value_caches, num_layers, src_dst_pairs,
                         num_pairs, src_num_blocks, dst_num_blocks, block_size, num_kv_heads, head_dim, dt, stream,
                         "swap_blocks");

@@ -35,9 +35,15 @@ def test_c_program_compiles_and_links(tmp_path):
 
 
 @pytest.mark.gpu
-def test_c_program_runs_one_decode_step(tmp_path):
+@pytest.mark.parametrize("nvtx", [False, True])
+def test_c_program_runs_one_decode_step(tmp_path, nvtx):
+    """nvtx: with PKV_NVTX set every launching call opens an NVTX range (a no-op without a tool)."""
     exe = build_program(tmp_path)
     env = dict(os.environ)
     env["LD_LIBRARY_PATH"] = os.path.dirname(pkv.LIB_PATH) + os.pathsep + env.get("LD_LIBRARY_PATH", "")
+    if nvtx:
+        env["PKV_NVTX"] = "1"
+    else:
+        env.pop("PKV_NVTX", None)
     r = subprocess.run([exe], capture_output=True, text=True, env=env, timeout=120)
     assert r.returncode == 0 and "abi_smoke ok" in r.stdout, r.stdout + r.stderr
