@@ -43,6 +43,10 @@ NOMINAL_HBM_GBS = 7900.0       # GB300 HBM3e nominal bandwidth: context beside t
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak); decode tokens/s"
 
 
+# the measured configurations, by number, and the workload each one runs
+CONFIGS = {1: "tiny", 2: "llama3_8b", 3: "llama2_70b_mixed_bs16", 4: "cow_fork", 5: "llama2_70b_step"}
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -54,6 +58,11 @@ def parse_args():
                         "batch; verify: the multi-query (speculative verify) call")
     p.add_argument("--num-queries", type=int, default=4, help="query tokens per sequence for --op verify")
     p.add_argument("--workload", default="llama3_8b", choices=sorted(W.SPECS))
+    p.add_argument("--config", type=int, choices=sorted(CONFIGS), default=None,
+                   help="the measured configurations by number (1 tiny, 2 8B-shaped, 3 70B-shaped mixed, "
+                        "4 copy-on-write forks, 5 80-layer 70B step); overrides --workload")
+    p.add_argument("--block-size", type=int, choices=[16, 32], default=None,
+                   help="with --config 3: the pool's block size (16 or 32)")
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
     p.add_argument("--ref-seconds", type=float, default=90.0, help="total budget of the --impl reference run")
@@ -66,7 +75,12 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--e2e-eager", action="store_true",
                    help="end-to-end loop issues every call from Python instead of replaying a CUDA graph of the step")
-    return p.parse_args()
+    args = p.parse_args()
+    if args.config is not None:
+        args.workload = CONFIGS[args.config]
+        if args.config == 3 and args.block_size == 32:
+            args.workload = "llama2_70b_mixed_bs32"
+    return args
 
 
 # ---------------------------------------------------------------- bytes
