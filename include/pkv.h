@@ -162,7 +162,8 @@ PKV_API int pkv_decode_plan_partition_tokens(const void* workspace, int num_seqs
  *                 first lists the (sequence, partition) items that exist,
  *                 longest sequences first, and with 0 picks the partition
  *                 size from the lengths themselves (about 0.85 x the
- *                 positions per resident CTA, multiples of 512, at least
+ *                 positions per resident CTA, an E4M3 position counting
+ *                 1.4 times, multiples of 512, at least
  *                 pkv_decode_partition_tokens); the output does not depend
  *                 on that order.
  * head_dim in {64, 128}; block_size in {8, 16, 32}; num_heads a multiple of
@@ -187,9 +188,10 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, const vo
  *
  * sum_seq_lens: the sum of seq_lens when the caller knows it (a scheduler
  * does), else 0.  It only sizes the decode grid: the work list then needs at
- * most num_seqs + sum_seq_lens / P entries (P the smallest partition size)
- * instead of num_seqs * ceil(max_seq_len / P), and a mixed-length batch
- * launches far fewer CTAs that find no work.  The plan kernel checks it
+ * most num_seqs + sum_seq_lens / P entries (P the smallest partition size the
+ * plan can pick, which with the automatic size the host derives from the
+ * same sum) instead of num_seqs * ceil(max_seq_len / P), and a mixed-length
+ * batch launches far fewer CTAs that find no work.  The plan kernel checks it
  * against the real sum; a wrong value raises the error word's bounds bit
  * (entries past the grid are then dropped and their outputs are undefined,
  * never out of range).
