@@ -310,6 +310,35 @@ def verify_attention_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.n
     return out
 
 
+def verify_attention_fp8_ref(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                             block_tables: np.ndarray, seq_lens: np.ndarray, scale: float, num_kv_heads: int,
+                             q_dtype: str, k_scale: np.ndarray, v_scale: np.ndarray) -> np.ndarray:
+    """Multi-query paged attention over an E4M3 pool; float64 [B, nq, num_heads, head_dim].
+
+    ``verify_attention_ref`` (P1 §4.4.2, P3 §4.2: the causal mask among the
+    query tokens) with the K/V of ``attention_fp8_ref`` (P3 §6.2: K_t =
+    e4m3_value(code) * k_scale[g], V_t = e4m3_value(code) * v_scale[g]).
+    q: fp16 / bf16 bits [B, nq, Hq, d]; caches uint8.
+    """
+    B, nq, Hq, d = q.shape
+    G = Hq // num_kv_heads
+    ks = np.asarray(k_scale, dtype=np.float32).astype(np.float64)
+    vs = np.asarray(v_scale, dtype=np.float32).astype(np.float64)
+    out = np.zeros((B, nq, Hq, d), dtype=np.float64)
+    for s in range(B):
+        L = int(seq_lens[s])
+        for g in range(num_kv_heads):
+            K = gather_sequence(key_cache, block_tables[s], L, g, E4M3) * ks[g]
+            V = gather_sequence(value_cache, block_tables[s], L, g, E4M3) * vs[g]
+            for i in range(nq):
+                vis = L - nq + i + 1
+                if L <= 0 or vis <= 0:
+                    continue
+                for h in range(g * G, (g + 1) * G):
+                    out[s, i, h] = softmax_attention(decode_bits(q[s, i, h], q_dtype), K[:vis], V[:vis], scale)
+    return out
+
+
 # --------------------------------------------------------------------------
 # split-K pieces: partial softmax over a slice of positions and its merge
 # --------------------------------------------------------------------------

@@ -110,9 +110,44 @@ def check_fp8_scales_act_where_stated():
     assert np.allclose(vh, base / 2, atol=1e-12)
 
 
+def check_fp8_verify_is_verify_on_dequantized_values():
+    """Verify (several causal query tokens) over the codes equals the unquantized
+    verify reference over the same values held exactly in fp16, token by token."""
+    rng = np.random.default_rng(6)
+    NB, bs, Hkv, d, Hq, nq = 10, 4, 2, 8, 6, 3
+    kcode = rng.integers(0x20, 0x50, size=(NB, bs, Hkv, d)).astype(np.uint8) | (rng.integers(0, 2, (NB, bs, Hkv, d)) << 7).astype(np.uint8)
+    vcode = rng.integers(0x20, 0x50, size=(NB, bs, Hkv, d)).astype(np.uint8)
+    ks = np.array([0.5, 4.0], np.float32)
+    vs = np.array([2.0, 0.25], np.float32)
+    kf = oracle.e4m3_value(kcode) * ks[None, None, :, None]
+    vf = oracle.e4m3_value(vcode) * vs[None, None, :, None]
+    tables = np.array([[6, 1, 9], [0, 5, 2], [4, 8, 3]], np.int32)
+    lens = np.array([11, 3, 2])                     # the last: fewer positions than query tokens
+    q = bits(rng.standard_normal((3, nq, Hq, d)))
+    got = oracle.verify_attention_fp8_ref(q, kcode, vcode, tables, lens, 0.3, Hkv, F16, ks, vs)
+    want = oracle.verify_attention_ref(q, bits(kf), bits(vf), tables, lens, 0.3, Hkv, F16)
+    assert np.allclose(got, want, rtol=0, atol=1e-12)
+    assert not got[2, 0].any()                      # query 0 of a 2-position sequence with 3 queries sees nothing
+
+
+def check_fp8_verify_one_query_is_decode():
+    """One query token per sequence: the single-query E4M3 reference."""
+    rng = np.random.default_rng(7)
+    kcode = rng.integers(0x28, 0x48, size=(6, 4, 1, 8)).astype(np.uint8)
+    vcode = rng.integers(0x28, 0x48, size=(6, 4, 1, 8)).astype(np.uint8)
+    tables = np.array([[2, 0, 3], [5, 4, 1]], np.int32)
+    lens = np.array([10, 7])
+    q = bits(rng.standard_normal((2, 1, 2, 8)))
+    one = np.array([1.5], np.float32)
+    got = oracle.verify_attention_fp8_ref(q, kcode, vcode, tables, lens, 0.2, 1, F16, one, one)
+    want = oracle.attention_fp8_ref(q[:, 0], kcode, vcode, tables, lens, 0.2, 1, F16, one, one)
+    assert np.array_equal(got[:, 0], want)
+
+
 FP8_PINS = [check_e4m3_known_codes, check_e4m3_quantize_rules, check_e4m3_quantize_matches_torch_cast,
             check_append_fp8_worked_example, check_fp8_attention_is_attention_on_dequantized_values,
-            check_fp8_scales_act_where_stated]
+            check_fp8_scales_act_where_stated, check_fp8_verify_is_verify_on_dequantized_values,
+            check_fp8_verify_one_query_is_decode]
 
 
 @pytest.mark.parametrize("pin", FP8_PINS, ids=lambda f: f.__name__)
