@@ -695,15 +695,21 @@ def run_verify(args, rank, world, local):
     k_new = torch.from_numpy(np.ascontiguousarray(wl.k_new).view(np.int16)).to(dev).view(tdt)
     v_new = torch.from_numpy(np.ascontiguousarray(wl.v_new).view(np.int16)).to(dev).view(tdt)
     slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    scales = {}
+    if spec.fp8:                                    # E4M3 pools: per-KV-head scales
+        scales = dict(k_scale=torch.from_numpy(wl.k_scales[0]).to(dev), v_scale=torch.from_numpy(wl.v_scales[0]).to(dev))
     for k, v in pools:                               # the step's new tokens, so every position holds one
-        pkv.paged_kv_append(k_new, v_new, k, v, slots)
+        if spec.fp8:
+            pkv.paged_kv_append_fp8(k_new, v_new, k, v, slots, scales["k_scale"], scales["v_scale"])
+        else:
+            pkv.paged_kv_append(k_new, v_new, k, v, slots)
     ws = pkv.alloc_workspace(B, Hq * nq, spec.num_kv_heads, d, wl.max_seq_len, args.partition_tokens, dev)
     nbytes = algorithmic_bytes(wl)["decode_unique"] + 2 * B * (nq - 1) * Hq * d * spec.elem_bytes
 
     def call(i):
         k, v = pools[i % replicas]
         pkv.paged_attention_verify(out, q, k, v, tables, lens, wl.scale, max_seq_len=wl.max_seq_len, workspace=ws,
-                                   partition_tokens=args.partition_tokens, sum_seq_lens=total_len)
+                                   partition_tokens=args.partition_tokens, sum_seq_lens=total_len, **scales)
 
     for i in range(max(3, args.warmup)):
         call(i)

@@ -336,6 +336,24 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, cons
                                           size_t workspace_bytes, int partition_tokens, void* stream);
 
 /*
+ * pkv_paged_attention_verify_fp8: pkv_paged_attention_verify over uint8 E4M3
+ * pools (P1 §4.4.2 and P3 §4.2: the draft tokens scored in one pass; P3 §6.2:
+ * over the low-precision K/V), with K and V as in
+ * pkv_paged_attention_decode_fp8 and the causal mask of
+ * pkv_paged_attention_verify.  q, out [num_seqs][num_queries][num_heads][128]
+ * in dt (PKV_F16 or PKV_BF16).  Query rows are served 8 per CTA, so a KV
+ * head with many rows streams its K/V once per 8 rows.
+ */
+PKV_API pkv_status pkv_paged_attention_verify_fp8(void* out, const void* q, const void* key_cache,
+                                          const void* value_cache, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                          int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                          int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                          float scale, pkv_dtype dt, const float* k_scale,
+                                          const float* v_scale, int num_queries, void* workspace,
+                                          size_t workspace_bytes, int partition_tokens, void* stream);
+
+/*
  * copy_blocks -- the copy-on-write block copy at a fork.
  *
  * P2 §3.1 (the scheduler output's blocks_to_copy, "用于 Copy-on-Write") and

@@ -32,7 +32,8 @@ ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_deco
                "pkv_bm_num_free_blocks", "pkv_bm_seq_len", "pkv_bm_refcount", "pkv_bm_allocate", "pkv_bm_fork",
                "pkv_bm_free", "pkv_bm_append_slots", "pkv_bm_block_tables", "pkv_paged_kv_append_fp8",
                "pkv_paged_attention_decode_fp8", "pkv_decode_plan", "pkv_paged_attention_decode_planned",
-               "pkv_paged_attention_decode_fp8_planned", "pkv_paged_kv_append_decode")
+               "pkv_paged_attention_decode_fp8_planned", "pkv_paged_kv_append_decode",
+               "pkv_paged_attention_verify_fp8")
 
 _lib = None
 
@@ -82,6 +83,9 @@ def load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode_planned.restype = c_i
     lib.pkv_paged_attention_decode_planned.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i,
                                                        c_i, c_i, c_i64, c_f, c_i, c_p, c_sz, c_i, c_p]
+    lib.pkv_paged_attention_verify_fp8.restype = c_i
+    lib.pkv_paged_attention_verify_fp8.argtypes = [c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i, c_i, c_i,
+                                                   c_i, c_i64, c_f, c_i, c_p, c_p, c_i, c_p, c_sz, c_i, c_p]
     lib.pkv_paged_kv_append_decode.restype = c_i
     lib.pkv_paged_kv_append_decode.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_i, c_p, c_i, c_i, c_i64, c_i,
                                                c_i, c_i, c_i, c_i64, c_f, c_i, c_i, c_p, c_p, c_p, c_sz, c_i, c_i, c_p]
@@ -341,10 +345,12 @@ def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, b
 
 
 def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,
-                           workspace=None, partition_tokens=0, sum_seq_lens=0) -> None:
+                           workspace=None, partition_tokens=0, sum_seq_lens=0, k_scale=None, v_scale=None) -> None:
     """Multi-query paged attention: q, out [B, nq, Hq, d]; query token i of sequence s attends over
-    positions [0, seq_lens[s] - nq + i] (the last nq positions are the queries' own K/V)."""
-    NB, bs, Hkv, d = _pool("key_cache", key_cache)
+    positions [0, seq_lens[s] - nq + i] (the last nq positions are the queries' own K/V).  uint8 pools
+    hold E4M3 codes and take k_scale / v_scale (float32 [Hkv]) as paged_attention_decode_fp8 does."""
+    kv8 = key_cache.dtype == torch.uint8
+    NB, bs, Hkv, d = _pool("key_cache", key_cache, tuple(_POOL_DT))
     if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
         raise ValueError("value_cache must match key_cache")
     if q.dim() != 4:
@@ -356,7 +362,8 @@ def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_len
         scale = 1.0 / math.sqrt(d)
     if max_seq_len is None:
         max_seq_len = int(seq_lens.max().item()) if B else 0
-    ptrs = [_cuda("out", out, key_cache.dtype), _cuda("q", q, key_cache.dtype), _cuda("key_cache", key_cache),
+    qdt = (torch.float16, torch.bfloat16) if kv8 else key_cache.dtype
+    ptrs = [_cuda("out", out, qdt), _cuda("q", q, out.dtype), _cuda("key_cache", key_cache),
             _cuda("value_cache", value_cache), _cuda("block_tables", block_tables, torch.int32, 2)]
     _cuda("seq_lens", seq_lens, torch.int32, 1)
     if block_tables.shape[0] != B or seq_lens.shape[0] != B:
@@ -365,10 +372,16 @@ def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_len
         workspace = alloc_workspace(B, Hq * nq, Hkv, d, int(max_seq_len), partition_tokens, q.device)
     ws_ptr = _cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().pkv_paged_attention_verify(
-        *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), int(sum_seq_lens),
-        Hq, Hkv, d, bs, NB, float(scale), _DT[key_cache.dtype], nq, ws_ptr, ws_bytes, int(partition_tokens),
-        _stream(q)))
+    lens_arg = [ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), int(sum_seq_lens)]
+    if kv8:
+        _check(load().pkv_paged_attention_verify_fp8(
+            *ptrs, block_tables.shape[1], *lens_arg, Hq, Hkv, d, bs, NB, float(scale), _DT[q.dtype],
+            _scales("k_scale", k_scale, Hkv), _scales("v_scale", v_scale, Hkv), nq, ws_ptr, ws_bytes,
+            int(partition_tokens), _stream(q)))
+    else:
+        _check(load().pkv_paged_attention_verify(
+            *ptrs, block_tables.shape[1], *lens_arg, Hq, Hkv, d, bs, NB, float(scale), _DT[key_cache.dtype], nq,
+            ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
 
 
 def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:

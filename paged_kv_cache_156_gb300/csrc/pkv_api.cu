@@ -291,8 +291,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     pkv_status st = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len);
     if (st != PKV_OK) return st;
     const bool kv8 = runs ? (k_scale || v_scale) : kv8_plan;    // an E4M3 pool (the _fp8 entry points)
-    if (kv8 && (head_dim != 128 || num_queries != 1))
-        return fail(PKV_ERR_UNSUPPORTED, "E4M3 pools: head_dim 128 and one query token only");
+    if (kv8 && head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "E4M3 pools: head_dim 128 only");
     if (num_queries < 1 || num_queries > 64) return fail(PKV_ERR_INVALID, "num_queries %d outside [1, 64]", num_queries);
     const int rows = num_heads * num_queries;            // query rows per sequence
     if (!valid_dtype(dt)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", static_cast<int>(dt));
@@ -370,7 +369,8 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.num_queries = num_queries;
     a.group = a.qgroup * num_queries;
     // more than kVerifyMinRows query rows per KV head: the verify kernel, 32 or 64 rows per CTA
-    const bool verify_kernel = num_queries > 1 && a.group > pkv::kVerifyMinRows;
+    // (E4M3 pools: the decode kernel's multi-query form, 8 rows per CTA, for any row count)
+    const bool verify_kernel = num_queries > 1 && a.group > pkv::kVerifyMinRows && !kv8;
     a.head_groups = verify_kernel ? (a.group + pkv::verify_rows_per_cta(a.group) - 1) / pkv::verify_rows_per_cta(a.group)
                                   : (a.group + 7) / 8;
     a.block_size = block_size;
@@ -445,6 +445,22 @@ pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt,
                           num_queries, workspace, workspace_bytes, partition_tokens, stream, nullptr, nullptr,
+                          pkv::DecodeMode::kPlanAndRun, false, sum_seq_lens);
+}
+
+pkv_status pkv_paged_attention_verify_fp8(void* out, const void* q, const void* key_cache, const void* value_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                          int num_seqs, int max_seq_len, int64_t sum_seq_lens, int num_heads,
+                                          int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                          float scale, pkv_dtype dt, const float* k_scale, const float* v_scale,
+                                          int num_queries, void* workspace, size_t workspace_bytes,
+                                          int partition_tokens, void* stream) {
+    CallRange range_("pkv_paged_attention_verify_fp8");
+    if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
+    if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "E4M3 pools need k_scale and v_scale");
+    return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                          max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt,
+                          num_queries, workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale,
                           pkv::DecodeMode::kPlanAndRun, false, sum_seq_lens);
 }
 

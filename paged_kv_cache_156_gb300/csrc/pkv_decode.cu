@@ -85,7 +85,7 @@ template <typename T, int D, int CW, int STAGES, bool MQ, bool KV8 = false>
 __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                      const __grid_constant__ CUtensorMap tmv,
                                                                      const DecodeArgs a) {
-    static_assert(!KV8 || (D == 128 && !MQ), "E4M3 pools: head_dim 128, one query token");
+    static_assert(!KV8 || D == 128, "E4M3 pools: head_dim 128");
     constexpr int kEB = KV8 ? 1 : 2;                // bytes of a pool element
     using G = Geo<D, CW, kEB>;
     using S = Smem<D, CW, STAGES, kEB>;
@@ -332,8 +332,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         const int nv = min(16, end - tokw);
         if (nv > 0) {
             if constexpr (KV8)
-                dec::consume_chunk_fp8<CW>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage), nv,
-                                           warp, lane, sl2);
+                dec::consume_chunk_fp8<CW, MQ>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage),
+                                               nv, warp, lane, sl2, tokw, lim0, lim1);
             else
                 dec::consume_chunk<T, D, CW, MQ>(ws, smem_u32(kring + st * G::kStage),
                                                  smem_u32(vring + st * G::kStage), nv, warp, lane, a.scale_log2, tokw,
@@ -410,7 +410,12 @@ int fp8_stages();
 template <typename T, int D>
 cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int warps, int stages,
                        cudaStream_t s) {
-    if (a.num_queries > 1) return launch_t<T, D, 4, 2, true>(a, tmk, tmv, s);   // verify: one shape
+    if (a.num_queries > 1) {                        // verify: one shape per pool type
+        if constexpr (D == 128)
+            if (a.kv8) return launch_t<T, D, 4, 4, true, true>(a, tmk, tmv, s);
+        if (a.kv8) return cudaErrorInvalidValue;
+        return launch_t<T, D, 4, 2, true>(a, tmk, tmv, s);
+    }
     if (a.kv8) {                                    // E4M3 pools: stages of 64 positions (8 KB each of K, V)
         if constexpr (D == 128) {
             switch (fp8_stages()) {

@@ -216,9 +216,9 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // V^T P^T the rows of tile mt are head-dim elements 16*g + 2*mt (row g) and
 // 16*g + 2*mt + 1 (row g + 8), g = lane / 4, so a lane reads 16 contiguous
 // bytes of each of its four positions; warp_state_to_smem_fp8 undoes it.
-template <int CW>
+template <int CW, bool MQ = false>
 __device__ __forceinline__ void consume_chunk_fp8(WarpState<128>& w, uint32_t kst, uint32_t vst, int nv, int warp,
-                                                  int lane, float sl2) {
+                                                  int lane, float sl2, int tokw = 0, int lim0 = 0, int lim1 = 0) {
     using M = Mma<__half>;
     const int g = lane >> 2, t = lane & 3;
     const int row0 = warp * 16 + g;
@@ -235,12 +235,13 @@ __device__ __forceinline__ void consume_chunk_fp8(WarpState<128>& w, uint32_t ks
         e4m3x4_to_f16x2x2(krb[ks], af[1], af[3]);
         M::run(sacc, af, w.qb[ks][0], w.qb[ks][1]);
     }
-    // ---- online softmax, as consume_chunk (one query token per sequence)
+    // ---- online softmax, as consume_chunk (verify: each column's causal limit)
     const bool va = g < nv, vb = g + 8 < nv;
-    const float s0 = va ? sacc[0] * sl2 : -INFINITY;
-    const float s1 = va ? sacc[1] * sl2 : -INFINITY;
-    const float s2 = vb ? sacc[2] * sl2 : -INFINITY;
-    const float s3 = vb ? sacc[3] * sl2 : -INFINITY;
+    const int pa = tokw + g, pb = pa + 8;
+    const float s0 = (va && (!MQ || pa < lim0)) ? sacc[0] * sl2 : -INFINITY;
+    const float s1 = (va && (!MQ || pa < lim1)) ? sacc[1] * sl2 : -INFINITY;
+    const float s2 = (vb && (!MQ || pb < lim0)) ? sacc[2] * sl2 : -INFINITY;
+    const float s3 = (vb && (!MQ || pb < lim1)) ? sacc[3] * sl2 : -INFINITY;
     float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -248,11 +249,14 @@ __device__ __forceinline__ void consume_chunk_fp8(WarpState<128>& w, uint32_t ks
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(w.m0, mx0), mn1 = fmaxf(w.m1, mx1);
-    const float al0 = fast_exp2(w.m0 - mn0), al1 = fast_exp2(w.m1 - mn1);
+    // verify: a column with no visible position yet keeps max -inf: scale 1, weights 0
+    const float al0 = (MQ && mn0 == -INFINITY) ? 1.0f : fast_exp2(w.m0 - mn0);
+    const float al1 = (MQ && mn1 == -INFINITY) ? 1.0f : fast_exp2(w.m1 - mn1);
     w.m0 = mn0;
     w.m1 = mn1;
-    const uint32_t p01 = M::pack(fast_exp2(s0 - mn0), fast_exp2(s1 - mn1));
-    const uint32_t p23 = M::pack(fast_exp2(s2 - mn0), fast_exp2(s3 - mn1));
+    const float b0 = (MQ && mn0 == -INFINITY) ? 0.0f : mn0, b1 = (MQ && mn1 == -INFINITY) ? 0.0f : mn1;
+    const uint32_t p01 = M::pack(fast_exp2(s0 - b0), fast_exp2(s1 - b1));
+    const uint32_t p23 = M::pack(fast_exp2(s2 - b0), fast_exp2(s3 - b1));
     const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);
     w.l0 = w.l0 * al0 + f01.x + f23.x;
     w.l1 = w.l1 * al1 + f01.y + f23.y;

@@ -142,3 +142,60 @@ def test_fp8_host_validation():
     assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
     with pytest.raises(ValueError):                        # one scale per KV head
         pkv.paged_attention_decode_fp8(torch.empty_like(q), q, k8, k8, tab, lens, one[:1], one, max_seq_len=1)
+
+
+VERIFY_CASES = [
+    dict(num_heads=32, num_kv_heads=8, block_size=16, dtype=W.BF16, nq=4, lens=("fixed", (4, 70, 1025, 300, 2))),
+    dict(num_heads=64, num_kv_heads=8, block_size=8, dtype=W.F16, nq=2, lens=("fixed", (2, 900, 129, 0))),
+    dict(num_heads=16, num_kv_heads=2, block_size=32, dtype=W.BF16, nq=5, lens=("fixed", (5, 3000, 64, 65))),
+    dict(num_heads=8, num_kv_heads=1, block_size=16, dtype=W.F16, nq=3, lens=("uniform", 3, 1500)),
+]
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 64, 1024])
+@pytest.mark.parametrize("case", range(len(VERIFY_CASES)))
+def test_verify_fp8_matches_oracle(case, partition_tokens):
+    """Several causal query tokens per sequence over E4M3 pools (rows per KV head from 4 to 40:
+    one and several 8-row groups); the last nq positions are the queries' own, appended first."""
+    kw = dict(VERIFY_CASES[case])
+    nq = kw.pop("nq")
+    kw["num_seqs"] = len(kw["lens"][1]) if kw["lens"][0] == "fixed" else 12
+    wl = W.build(W.small_spec(seed=840 + case, head_dim=128, kv_dtype=W.E4M3, **kw))
+    s = wl.spec
+    dk, dv = cuda_of(wl.key_caches[0]), cuda_of(wl.value_caches[0])
+    ks, vs = wl.k_scales[0], wl.v_scales[0]
+    pkv.paged_kv_append_fp8(to_dev(wl.k_new, s.dtype), to_dev(wl.v_new, s.dtype), dk, dv, cuda_of(wl.slot_mapping),
+                            f32(ks), f32(vs))
+    rng = np.random.default_rng(850 + case)
+    q = W.normal_bits(rng, (s.num_seqs, nq, s.num_heads, s.head_dim), s.dtype)
+    qd = to_dev(q, s.dtype)
+    out = torch.full_like(qd, float("nan"))
+    pkv.paged_attention_verify(out, qd, dk, dv, cuda_of(wl.block_tables), cuda_of(wl.seq_lens), wl.scale,
+                               max_seq_len=wl.max_seq_len, partition_tokens=partition_tokens,
+                               sum_seq_lens=int(wl.seq_lens.sum()), k_scale=f32(ks), v_scale=f32(vs))
+    torch.cuda.synchronize()
+    kc, vc = wl.key_caches[0].copy(), wl.value_caches[0].copy()
+    oracle.append_fp8_ref(kc, vc, wl.k_new, wl.v_new, wl.slot_mapping, ks, vs, s.dtype)
+    ref = oracle.verify_attention_fp8_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype,
+                                          ks, vs)
+    assert torch.isfinite(out).all()
+    err = max_abs_err(out, ref)
+    assert err <= TOL[s.dtype], f"max abs err {err}"
+
+
+def test_verify_fp8_one_query_is_the_decode_call():
+    wl = W.build(W.small_spec(num_seqs=5, num_heads=32, num_kv_heads=8, head_dim=128, dtype=W.BF16, seed=860,
+                              kv_dtype=W.E4M3, lens=("fixed", (900, 33, 2049, 1, 4000))))
+    s = wl.spec
+    dk, dv = cuda_of(wl.key_caches[0]), cuda_of(wl.value_caches[0])
+    ks, vs = f32(wl.k_scales[0]), f32(wl.v_scales[0])
+    q = to_dev(wl.q, s.dtype)
+    tab, lens = cuda_of(wl.block_tables), cuda_of(wl.seq_lens)
+    a = torch.empty_like(q)
+    pkv.paged_attention_decode_fp8(a, q, dk, dv, tab, lens, ks, vs, wl.scale, max_seq_len=wl.max_seq_len,
+                                   partition_tokens=256)
+    b = torch.empty_like(q).unsqueeze(1)
+    pkv.paged_attention_verify(b, q.unsqueeze(1).contiguous(), dk, dv, tab, lens, wl.scale,
+                               max_seq_len=wl.max_seq_len, partition_tokens=256, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b[:, 0].view(torch.int16))
