@@ -40,7 +40,8 @@ namespace {
 
 pkv_status err(pkv_status st, const char* msg) { return static_cast<pkv_status>(pkv::set_error_message(st, msg)); }
 
-int64_t blocks_for(int64_t tokens, int bs) { return (tokens + bs - 1) / bs; }
+// ceil(tokens / bs) without forming tokens + bs - 1, which overflows near INT64_MAX
+int64_t blocks_for(int64_t tokens, int bs) { return tokens / bs + (tokens % bs != 0); }
 
 }  // namespace
 
@@ -189,6 +190,8 @@ pkv_status pkv_bm_block_tables(const pkv_block_manager* bm, const int64_t* seq_i
         if (it == bm->seqs.end()) return err(PKV_ERR_INVALID, "block_tables: unknown sequence");
         if (static_cast<int64_t>(it->second.blocks.size()) > max_blocks_per_seq)
             return err(PKV_ERR_INVALID, "block_tables: max_blocks_per_seq too small");
+        if (it->second.num_tokens > INT32_MAX)
+            return err(PKV_ERR_INVALID, "block_tables: a sequence length does not fit int32 seq_lens");
     }
     for (int64_t i = 0; i < n; ++i) {
         const auto& sq = bm->seqs.find(seq_ids[i])->second;

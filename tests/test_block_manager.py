@@ -99,6 +99,19 @@ def test_invalid_calls():
         pkv.BlockManager(4, 16, free_order=[0, 1, 1, 3])
 
 
+def test_huge_allocation_is_refused_whole():
+    """ceil(tokens / block_size) must not overflow: a request for INT64_MAX
+    tokens needs more blocks than any pool holds, so it fails and takes none."""
+    bm = pkv.BlockManager(8, 16)
+    for n in (2 ** 63 - 1, 2 ** 63 - 16, 9 * 16):
+        with pytest.raises(pkv.PkvError) as e:
+            bm.allocate(1, n)
+        assert e.value.status == pkv.PKV_ERR_OOM
+        assert bm.seq_len(1) == -1 and bm.num_free_blocks == 8
+    bm.allocate(1, 8 * 16)                   # exactly the pool
+    assert bm.num_free_blocks == 0
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_random_operations_match_reference(seed):
     rng = np.random.default_rng(seed)
