@@ -35,14 +35,15 @@ using dec::kMaxTable;
 
 constexpr int kVW = 4;                 // consumer warps
 constexpr int kVRows = 16 * kVW;       // query rows per CTA
-constexpr int kVStages = 2;
+constexpr int kWholeStages = 2;        // K/V ring depth of the 64-row kernel (chunks)
+constexpr int kSplitStages = 3;        // and of the 32-row kernel
 
-template <int D>
+template <int D, int STAGES>
 struct VSmem {
     using G = Geo<D, kVW>;
-    static constexpr size_t kRing = 2 * kVStages * G::kStage;
+    static constexpr size_t kRing = 2 * STAGES * G::kStage;
     static constexpr size_t kBars = kRing;
-    static constexpr size_t kTable = kBars + (2 * kVStages + 1) * sizeof(uint64_t);
+    static constexpr size_t kTable = kBars + (2 * STAGES + 1) * sizeof(uint64_t);
     static constexpr size_t kMisc = kTable + kMaxTable * sizeof(int);
     static constexpr size_t kBytes = kMisc + 16;
 };
@@ -55,13 +56,14 @@ __device__ __forceinline__ int64_t vrow_offset(const DecodeArgs& a, int s, int k
 }
 
 // SPLIT: warps sharing one 16-row tile (1: 64 rows per CTA; 2: 32 rows, each
-// warp takes half of every chunk's positions).
-template <typename T, int D, int SPLIT>
+// warp takes half of every chunk's positions).  STAGES: depth of the K/V ring.
+template <typename T, int D, int SPLIT, int STAGES>
 __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                           const __grid_constant__ CUtensorMap tmv,
                                                                           const DecodeArgs a) {
+    constexpr int kVStages = STAGES;
     using G = Geo<D, kVW>;
-    using S = VSmem<D>;
+    using S = VSmem<D, STAGES>;
     using M = Mma<T>;
     constexpr int kChunk = G::kChunk;               // 64 positions
     constexpr int kNT = kChunk / 8 / SPLIT;         // n-tiles of S per chunk and warp
@@ -166,7 +168,10 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
         if (lane == 0 && !*abort_flag) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-            const uint64_t pol = l2_policy_evict_first();   // K/V read once: keep the reused data in L2
+            // K/V read once: keep the reused data in L2.  With more than one
+            // row group per KV head the sibling CTAs read the same tiles: no hint.
+            const bool hint = a.head_groups == 1;
+            const uint64_t pol = l2_policy_evict_first();
             const int per_chunk = kChunk / bs;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % kVStages;
@@ -183,8 +188,13 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
 #pragma unroll
                     for (int hf = 0; hf < G::kHalves; ++hf) {
                         const int off = st * G::kStage + hf * G::kPlane + j * bs * 128;
-                        tma_load_4d_hint(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st], pol);
-                        tma_load_4d_hint(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st], pol);
+                        if (hint) {
+                            tma_load_4d_hint(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st], pol);
+                            tma_load_4d_hint(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st], pol);
+                        } else {
+                            tma_load_4d(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st]);
+                            tma_load_4d(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st]);
+                        }
                     }
                 }
             }
@@ -476,14 +486,13 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
     }
 }
 
-template <typename T, int D>
-cudaError_t launch_verify_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
-    constexpr size_t smem = VSmem<D>::kBytes;
-    static_assert(smem <= 232448, "shared memory budget");
-    static_assert(2 * 32 * (D / 8 * 4 + 4) * sizeof(float) <= 2 * kVStages * Geo<D, kVW>::kStage,
+template <typename T, int D, int SPLIT, int STAGES>
+cudaError_t launch_verify_k(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
+    constexpr size_t smem = VSmem<D, STAGES>::kBytes;
+    static_assert(2 * smem + 2048 <= 233472, "two CTAs per SM fit the shared memory");
+    static_assert(2 * 32 * (D / 8 * 4 + 4) * sizeof(float) <= 2 * STAGES * Geo<D, kVW>::kStage,
                   "the half-merge scratch fits the ring");
-    // 32 rows per CTA: two warps per 16-row tile; 64: one warp per tile (head_groups matches)
-    auto kern = verify_rows_per_cta(a.group) == kVRows / 2 ? verify_kernel<T, D, 2> : verify_kernel<T, D, 1>;
+    auto kern = verify_kernel<T, D, SPLIT, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
@@ -499,6 +508,17 @@ cudaError_t launch_verify_t(const DecodeArgs& a, const CUtensorMap& tmk, const C
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
+}
+
+template <typename T, int D>
+cudaError_t launch_verify_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
+    // 32 rows per CTA: two warps per 16-row tile; 64: one warp per tile (head_groups matches)
+    // (a 3-chunk ring for the 32-row kernel, whose warps each take half a chunk
+    // and so wait on the ring sooner; 2 chunks for 64 rows, where the extra
+    // stage measured no faster)
+    const bool split = verify_rows_per_cta(a.group) == kVRows / 2;
+    return split ? launch_verify_k<T, D, 2, kSplitStages>(a, tmk, tmv, s)
+                 : launch_verify_k<T, D, 1, kWholeStages>(a, tmk, tmv, s);
 }
 
 }  // namespace
@@ -542,8 +562,7 @@ int verify_ctas_per_sm(int head_dim, int rows) {
     const int i = (head_dim == 64 ? 0 : 1) + (split ? 2 : 0);
     if (cache[i] < 0) {
         int n = 0;
-        const size_t smem = head_dim == 64 ? VSmem<64>::kBytes : VSmem<128>::kBytes;
-        auto set_and_query = [&](auto kern) {
+        auto set_and_query = [&](auto kern, size_t smem) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
                     cudaSuccess &&
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Geo<128, kVW>::kThreads, smem) == cudaSuccess)
@@ -551,10 +570,10 @@ int verify_ctas_per_sm(int head_dim, int rows) {
             return 0;
         };
         switch (i) {
-            case 0: cache[i] = set_and_query(verify_kernel<__half, 64, 1>); break;
-            case 1: cache[i] = set_and_query(verify_kernel<__half, 128, 1>); break;
-            case 2: cache[i] = set_and_query(verify_kernel<__half, 64, 2>); break;
-            default: cache[i] = set_and_query(verify_kernel<__half, 128, 2>); break;
+            case 0: cache[i] = set_and_query(verify_kernel<__half, 64, 1, kWholeStages>, VSmem<64, kWholeStages>::kBytes); break;
+            case 1: cache[i] = set_and_query(verify_kernel<__half, 128, 1, kWholeStages>, VSmem<128, kWholeStages>::kBytes); break;
+            case 2: cache[i] = set_and_query(verify_kernel<__half, 64, 2, kSplitStages>, VSmem<64, kSplitStages>::kBytes); break;
+            default: cache[i] = set_and_query(verify_kernel<__half, 128, 2, kSplitStages>, VSmem<128, kSplitStages>::kBytes); break;
         }
     }
     return cache[i];
