@@ -1,8 +1,9 @@
 """Python binding of the paged KV-cache decode library (``_lib/libpkv.so``).
 
-Argument marshalling only: every function checks tensor placement, dtype,
-shape and contiguity, then passes raw device pointers and the current CUDA
-stream to the C ABI declared in ``include/pkv.h``.  All work runs in the
+Argument marshalling only: every function checks tensor placement (all of a
+call's CUDA tensors on one device, made current for the call), dtype, shape
+and contiguity, then passes raw device pointers and that device's current
+CUDA stream to the C ABI declared in ``include/pkv.h``.  All work runs in the
 library's CUDA kernels; there is no CPU path.  A missing library raises.
 
     paged_kv_append(k, v, key_cache, value_cache, slot_mapping)
@@ -12,6 +13,7 @@ library's CUDA kernels; there is no CPU path.  A missing library raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 
@@ -126,6 +128,32 @@ def _check(status: int):
         raise PkvError(status, load().pkv_last_error().decode(errors="replace"))
 
 
+def _cuda_devices(values):
+    """The CUDA devices of the tensors among ``values`` (tensors, or lists / tuples of them)."""
+    devs = set()
+    for v in values:
+        for t in (v if isinstance(v, (list, tuple)) else (v,)):
+            if isinstance(t, torch.Tensor) and t.is_cuda:
+                devs.add(t.device)
+    return devs
+
+
+def _one_device(fn):
+    """Every CUDA tensor of the call on one device, and that device current while
+    the library runs: the kernels launch on the current device, on the stream of
+    the tensors' device, and dereference every pointer there."""
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        devs = _cuda_devices(list(args) + list(kwargs.values()))
+        if len(devs) > 1:
+            raise ValueError(f"{fn.__name__}: tensors on more than one device: {sorted(str(d) for d in devs)}")
+        if not devs:
+            return fn(*args, **kwargs)
+        with torch.cuda.device(devs.pop()):
+            return fn(*args, **kwargs)
+    return call
+
+
 def _stream(t: torch.Tensor):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
@@ -147,6 +175,7 @@ def _pool(name, c, dtypes=(torch.float16, torch.bfloat16)):
     return c.shape  # num_blocks, block_size, num_kv_heads, head_dim
 
 
+@_one_device
 def paged_kv_append(k, v, key_cache, value_cache, slot_mapping) -> None:
     """Write k[t], v[t] ([T, Hkv, d]) into slot slot_mapping[t] (int64; < 0 = skip)."""
     NB, bs, Hkv, d = _pool("key_cache", key_cache)
@@ -164,6 +193,7 @@ def decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_dim, max_seq
     return int(load().pkv_decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len))
 
 
+@_one_device
 def decode_plan_partition_tokens(workspace, num_seqs, num_heads, num_kv_heads) -> int:
     """Partition size the last decode call with ``workspace`` used (-1: unplanned batch); synchronises."""
     return int(load().pkv_decode_plan_partition_tokens(_cuda("workspace", workspace), num_seqs, num_heads,
@@ -183,6 +213,7 @@ def alloc_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_seq_len, pa
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+@_one_device
 def decode_plan(workspace, block_tables, seq_lens, num_heads, key_cache, max_seq_len, partition_tokens=0,
                 sum_seq_lens=0) -> None:
     """The work list of a decode batch, once per step (``pkv_decode_plan``): the runs that pass
@@ -201,6 +232,7 @@ def decode_plan(workspace, block_tables, seq_lens, num_heads, key_cache, max_seq
                                   _stream(workspace)))
 
 
+@_one_device
 def paged_attention_decode(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, block_size=None,
                            num_kv_heads=None, max_seq_len=None, workspace=None, partition_tokens=0,
                            planned=False, sum_seq_lens=0) -> None:
@@ -253,6 +285,7 @@ def _scales(name, t, Hkv):
     return ctypes.c_void_p(t.data_ptr())
 
 
+@_one_device
 def paged_kv_append_fp8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_scale) -> None:
     """Quantize k[t], v[t] ([T, Hkv, d], fp16 / bf16) into slot slot_mapping[t] of uint8 E4M3 pools:
     code = e4m3(float32(x) / scale[head]) (nearest even, saturating); k_scale, v_scale float32 [Hkv]."""
@@ -270,6 +303,7 @@ def paged_kv_append_fp8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_s
                                           _scales("v_scale", v_scale, Hkv), _stream(key_cache)))
 
 
+@_one_device
 def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq_lens, k_scale, v_scale, scale=None,
                                max_seq_len=None, workspace=None, partition_tokens=0, planned=False,
                                sum_seq_lens=0) -> None:
@@ -304,6 +338,7 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq
         _check(load().pkv_paged_attention_decode_fp8(*ptrs, block_tables.shape[1], *lens_arg, *rest))
 
 
+@_one_device
 def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, block_tables, seq_lens, scale=None,
                            max_seq_len=None, workspace=None, partition_tokens=0, planned=False, sum_seq_lens=0,
                            k_scale=None, v_scale=None) -> None:
@@ -344,6 +379,7 @@ def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, b
         int(partition_tokens), int(bool(planned)), _stream(q)))
 
 
+@_one_device
 def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_lens, scale=None, max_seq_len=None,
                            workspace=None, partition_tokens=0, sum_seq_lens=0, k_scale=None, v_scale=None) -> None:
     """Multi-query paged attention: q, out [B, nq, Hq, d]; query token i of sequence s attends over
@@ -384,6 +420,7 @@ def paged_attention_verify(out, q, key_cache, value_cache, block_tables, seq_len
             ws_ptr, ws_bytes, int(partition_tokens), _stream(q)))
 
 
+@_one_device
 def copy_blocks(key_caches, value_caches, src_dst_pairs) -> None:
     """For each (src, dst) row of src_dst_pairs (int64 [Np, 2]): every layer's block dst = block src."""
     if isinstance(key_caches, torch.Tensor):
@@ -418,6 +455,7 @@ def _addressable_pool(name, t):
     return t.data_ptr()
 
 
+@_one_device
 def swap_blocks(src_key_caches, src_value_caches, dst_key_caches, dst_value_caches, src_dst_pairs) -> None:
     """dst[dst_i] = src[src_i] for every (src_i, dst_i) row of src_dst_pairs (int64 [Np, 2], on the GPU),
     for every layer's K and V pool.  Pools are CUDA tensors or pinned host tensors (swap out / swap in)."""

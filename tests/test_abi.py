@@ -125,3 +125,35 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         pkv.paged_kv_append(torch.zeros(1, 2, 64, dtype=torch.float16), torch.zeros(1, 2, 64, dtype=torch.float16),
                             t, t, torch.zeros(1, dtype=torch.int64))
+
+
+def test_binding_refuses_tensors_on_two_devices(lib):
+    """Every CUDA tensor of one call must sit on one device (the kernels run on
+    that device and dereference every pointer there).  Stand-in tensors that
+    report a CUDA device let this run without a GPU: the check raises before
+    any pointer is read."""
+    import torch
+
+    class OnDevice(torch.Tensor):
+        @property
+        def is_cuda(self):
+            return True
+
+        @property
+        def device(self):
+            return self._dev
+
+    def on(i, shape=(1,)):
+        t = torch.Tensor._make_subclass(OnDevice, torch.zeros(shape))
+        t._dev = torch.device("cuda", i)
+        return t
+
+    assert pkv._cuda_devices([on(0), [on(1), torch.zeros(1)], None, 3]) == {torch.device("cuda", 0),
+                                                                               torch.device("cuda", 1)}
+    assert pkv._cuda_devices([torch.zeros(1), [torch.zeros(1)]]) == set()
+    with pytest.raises(ValueError, match="more than one device"):
+        pkv.paged_kv_append(on(0), on(0), on(1), on(1), on(0))
+    with pytest.raises(ValueError, match="more than one device"):
+        pkv.copy_blocks([on(0)], [on(1)], on(0))
+    with pytest.raises(ValueError, match="more than one device"):
+        pkv.paged_attention_decode(on(0), on(0), on(0), on(0), on(0), on(1), max_seq_len=1)
