@@ -24,6 +24,8 @@
 // decode (the last partition merges).
 #include <stdlib.h>
 
+#include <atomic>
+
 #include "pkv_decode_common.cuh"
 
 namespace pkv {
@@ -557,10 +559,12 @@ int verify_rows_per_cta(int rows) {
 }
 
 int verify_ctas_per_sm(int head_dim, int rows) {
-    static int cache[4] = {-1, -1, -1, -1};
+    // the same on every GB300; threads that race here store the same value
+    static std::atomic<int> cache[4] = {-1, -1, -1, -1};
     const bool split = verify_rows_per_cta(rows) == kVRows / 2;
     const int i = (head_dim == 64 ? 0 : 1) + (split ? 2 : 0);
-    if (cache[i] < 0) {
+    int n_cached = cache[i].load(std::memory_order_relaxed);
+    if (n_cached < 0) {
         int n = 0;
         auto set_and_query = [&](auto kern, size_t smem) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
@@ -570,13 +574,14 @@ int verify_ctas_per_sm(int head_dim, int rows) {
             return 0;
         };
         switch (i) {
-            case 0: cache[i] = set_and_query(verify_kernel<__half, 64, 1, kWholeStages>, VSmem<64, kWholeStages>::kBytes); break;
-            case 1: cache[i] = set_and_query(verify_kernel<__half, 128, 1, kWholeStages>, VSmem<128, kWholeStages>::kBytes); break;
-            case 2: cache[i] = set_and_query(verify_kernel<__half, 64, 2, kSplitStages>, VSmem<64, kSplitStages>::kBytes); break;
-            default: cache[i] = set_and_query(verify_kernel<__half, 128, 2, kSplitStages>, VSmem<128, kSplitStages>::kBytes); break;
+            case 0: n_cached = set_and_query(verify_kernel<__half, 64, 1, kWholeStages>, VSmem<64, kWholeStages>::kBytes); break;
+            case 1: n_cached = set_and_query(verify_kernel<__half, 128, 1, kWholeStages>, VSmem<128, kWholeStages>::kBytes); break;
+            case 2: n_cached = set_and_query(verify_kernel<__half, 64, 2, kSplitStages>, VSmem<64, kSplitStages>::kBytes); break;
+            default: n_cached = set_and_query(verify_kernel<__half, 128, 2, kSplitStages>, VSmem<128, kSplitStages>::kBytes); break;
         }
+        cache[i].store(n_cached, std::memory_order_relaxed);
     }
-    return cache[i];
+    return n_cached;
 }
 
 }  // namespace pkv
