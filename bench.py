@@ -63,6 +63,8 @@ def parse_args():
                         "4 copy-on-write forks, 5 80-layer 70B step); overrides --workload")
     p.add_argument("--block-size", type=int, choices=[16, 32], default=None,
                    help="with --config 3: the pool's block size (16 or 32)")
+    p.add_argument("--dtype", choices=["f16", "bf16"], default=None,
+                   help="16-bit type of q, out and the pools (default: the workload's own)")
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the cpu_baseline sample")
     p.add_argument("--ref-seconds", type=float, default=90.0, help="total budget of the --impl reference run")
@@ -81,6 +83,15 @@ def parse_args():
         if args.config == 3 and args.block_size == 32:
             args.workload = "llama2_70b_mixed_bs32"
     return args
+
+
+def workload_spec(args) -> W.Spec:
+    """The named workload, in the 16-bit type --dtype names when given."""
+    spec = W.SPECS[args.workload]
+    if args.dtype and args.dtype != spec.dtype:
+        spec = dataclasses.replace(spec, dtype=args.dtype,
+                                   description=f"{spec.description} (run in {args.dtype})")
+    return spec
 
 
 # ---------------------------------------------------------------- bytes
@@ -269,7 +280,7 @@ def run_pkv(args, rank, world, local):
     pkv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = W.SPECS[args.workload]
+    spec = workload_spec(args)
     if args.layers and spec.num_layers > 1:
         spec = dataclasses.replace(spec, num_layers=min(args.layers, spec.num_layers))
     wl = W.build(spec, values="none")
@@ -529,7 +540,7 @@ def run_pkv(args, rank, world, local):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    spec = W.SPECS[args.workload]
+    spec = workload_spec(args)
     wl = W.build(spec, values="none")
     seqs = sample_for_oracle(wl, 4)
     pools = W.host_pools_for(wl, seqs, 0)
@@ -575,7 +586,7 @@ def run_swap(args, rank, world, local):
     pkv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = W.SPECS[args.workload]
+    spec = workload_spec(args)
     wl = W.build(spec, values="none")
     tdt = torch.float16 if spec.dtype == W.F16 else torch.bfloat16
     bs = spec.block_size
@@ -674,7 +685,7 @@ def run_verify(args, rank, world, local):
     pkv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = W.SPECS[args.workload]
+    spec = workload_spec(args)
     if spec.num_layers != 1:
         raise SystemExit("--op verify runs single-layer workloads")
     wl = W.build(spec, values="none")

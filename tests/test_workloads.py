@@ -95,3 +95,18 @@ def test_e4m3_pools_finite_where_valid_and_poisoned_elsewhere():
         assert np.all(kc[~wl.valid_slots] == W.E4M3_NAN)
     assert len(wl.k_scales) == 1 and wl.k_scales[0].dtype == np.float32 and np.all(wl.k_scales[0] > 0)
     assert wl.pool_bytes_per_layer() == 2 * int(np.prod(wl.pool_shape()))
+
+
+def test_bench_dtype_override():
+    """bench.py --dtype runs a workload in the other 16-bit type, everything else unchanged."""
+    import argparse
+    import bench
+
+    for name in ("llama3_8b", "llama2_70b_mixed_bs16", "llama3_8b_fp8"):
+        base = W.SPECS[name]
+        for dt in (W.F16, W.BF16):
+            s = bench.workload_spec(argparse.Namespace(workload=name, dtype=dt))
+            assert s.dtype == dt and s.kv_dtype == base.kv_dtype
+            assert (s.num_seqs, s.num_heads, s.num_kv_heads, s.head_dim, s.block_size, s.seed, s.lens) == \
+                (base.num_seqs, base.num_heads, base.num_kv_heads, base.head_dim, base.block_size, base.seed, base.lens)
+        assert bench.workload_spec(argparse.Namespace(workload=name, dtype=None)) is base
