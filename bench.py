@@ -136,6 +136,28 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def verify_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pkv_verify.cu", "pkv_decode_common.cuh", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_156_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_verify_traffic(workload: str, num_queries: int):
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu summary for
+    this workload and query count, or None (no summary, or the sources changed)."""
+    path = os.path.join(ROOT, "profiles", f"verify_{workload}_nq{num_queries}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m_h = re.search(r"verify_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != verify_source_hash():
+        return None
+    return int(m_t.group(1))
+
+
 def profiled_traffic(workload: str):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
     or None when there is none or the kernel source changed since the capture."""
@@ -748,7 +770,9 @@ def run_verify(args, rank, world, local):
                        "l2": f"{replicas} rotating pool replicas"},
             "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(gbs / world / peak, 4), "nominal_peak": NOMINAL_HBM_GBS,
-                         "frac_of_nominal": round(gbs / world / NOMINAL_HBM_GBS, 4)},
+                         "frac_of_nominal": round(gbs / world / NOMINAL_HBM_GBS, 4),
+                         "traffic": profiled_verify_traffic(spec.name, nq),
+                         "algorithmic_bytes_per_launch": int(nbytes)},
             "gpu_launches": 2 * args.steps}
 
 
