@@ -688,7 +688,8 @@ def run_swap(args, rank, world, local):
                          "peak": round(ce_gbs, 2), "peak_kind": "measured: copy engines, same bytes, contiguous",
                          "unit": "GB/s", "frac": round(step_bytes / ((out_ms + in_ms) / 1e3) / 1e9 / ce_gbs, 4),
                          "copy_engine_out_GBps": round(nb * block_bytes / (ce_out / 1e3) / 1e9, 2),
-                         "copy_engine_in_GBps": round(nb * block_bytes / (ce_in / 1e3) / 1e9, 2)},
+                         "copy_engine_in_GBps": round(nb * block_bytes / (ce_in / 1e3) / 1e9, 2),
+                         "traffic": None},   # bounded by the host link, not by DRAM: no ncu DRAM figure applies
             "gpu_launches": 2 * args.steps * ((layers + 63) // 64)}
 
 
