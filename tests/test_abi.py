@@ -102,6 +102,27 @@ def test_fused_and_verify_validation_rejects_before_launch(lib):
                                         null, 0, 0, null)
     assert st == pkv.PKV_ERR_INVALID
 
+    def verify(nq=4, head_dim=128, ptr=fake):
+        # out, q, key_cache, value_cache, tables, width, lens, B, max_len, sum, Hq, Hkv, d, bs, num_blocks, scale, dt,
+        # num_queries, workspace, workspace_bytes, partition, stream
+        return lib.pkv_paged_attention_verify(ptr, fake, fake, fake, fake, 4, fake, 2, 10, 0, 8, 2, head_dim, 16, 10,
+                                              1.0, 0, nq, null, 0, 0, null)
+
+    for nq in (0, -1, 65):                  # query tokens per sequence in [1, 64]
+        assert verify(nq=nq) == pkv.PKV_ERR_INVALID and b"num_queries" in lib.pkv_last_error()
+    assert verify(head_dim=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert verify(ptr=null) == pkv.PKV_ERR_INVALID
+
+    def verify_fp8(k_scale=fake, v_scale=fake, head_dim=128, sum_lens=0):
+        # as verify, with the scales before num_queries
+        return lib.pkv_paged_attention_verify_fp8(fake, fake, fake, fake, fake, 4, fake, 2, 10, sum_lens, 8, 2,
+                                                  head_dim, 16, 10, 1.0, 0, k_scale, v_scale, 4, null, 0, 0, null)
+
+    assert verify_fp8(k_scale=null) == pkv.PKV_ERR_INVALID and b"k_scale" in lib.pkv_last_error()
+    assert verify_fp8(v_scale=null) == pkv.PKV_ERR_INVALID
+    assert verify_fp8(sum_lens=-5) == pkv.PKV_ERR_INVALID
+    assert verify_fp8(head_dim=64) == pkv.PKV_ERR_UNSUPPORTED         # E4M3 pools: head_dim 128
+
 
 def test_workspace_formula(lib):
     # explicit partition sizes need no device query
