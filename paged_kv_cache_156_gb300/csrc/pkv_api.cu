@@ -144,7 +144,7 @@ int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_se
     int p = 1024;
     while (p < kMaxPartition && (max_seq_len + p - 1) / p > 512) p <<= 1;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads * head_groups;
-    const int64_t slots = static_cast<int64_t>(sms > 0 ? sms : 148) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    const int64_t slots = static_cast<int64_t>(sms > 0 ? sms : 152) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
     auto waves = [&](int q) { return static_cast<double>(pairs * ((max_seq_len + q - 1) / q)) / slots; };
     if (p == 1024 && waves(1024) >= 1.0 && waves(1024) < 3.0) {
         double best = -1.0;
@@ -159,7 +159,7 @@ int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_se
         }
         return best_p;
     }
-    while (p > 128 && pairs * ((max_seq_len + p - 1) / p) < 2LL * (sms > 0 ? sms : 148)) p >>= 1;
+    while (p > 128 && pairs * ((max_seq_len + p - 1) / p) < 2LL * (sms > 0 ? sms : 152)) p >>= 1;
     return p;
 }
 

@@ -178,3 +178,21 @@ def test_binding_refuses_tensors_on_two_devices(lib):
         pkv.copy_blocks([on(0)], [on(1)], on(0))
     with pytest.raises(ValueError, match="more than one device"):
         pkv.paged_attention_decode(on(0), on(0), on(0), on(0), on(0), on(1), max_seq_len=1)
+
+
+def test_host_partition_rule_properties(lib):
+    """The host's smallest partition size (pkv_decode_partition_tokens) over a grid
+    of batch shapes, including 0 sequences, length 0 and lengths far past any
+    configuration: always a multiple of 64 in [128, 4096], the range the decode
+    call accepts, and the workspace for it is defined.  Without a GPU the rule
+    takes 152 SMs and one resident CTA per SM."""
+    for B in (0, 1, 4, 16, 64, 128, 768, 65535):
+        for Hq, Hkv in ((4, 4), (32, 8), (64, 8), (8, 1)):
+            for L in (0, 1, 50, 1024, 4096, 8192, 100000, 2 ** 21):
+                for d in (64, 128):
+                    p = lib.pkv_decode_partition_tokens(B, Hq, Hkv, d, L)
+                    assert p % 64 == 0 and 128 <= p <= 4096, (B, Hq, Hkv, L, d, p)
+                    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, L, p) != ctypes.c_size_t(-1).value
+    assert lib.pkv_decode_partition_tokens(4, 6, 4, 128, 100) < 0        # heads not a multiple of KV heads
+    assert lib.pkv_decode_partition_tokens(4, 8, 2, 96, 100) < 0         # head_dim not built
+
