@@ -106,13 +106,3 @@ def max_abs_err(gpu_out: torch.Tensor, ref: np.ndarray, seqs=None) -> float:
     if seqs is not None:
         g = g[np.asarray(seqs)]
     return float(np.max(np.abs(g - ref))) if g.size else 0.0
-
-
-def sample_seqs(wl: W.Workload, n: int = 6, seed: int = 0):
-    """The longest and shortest sequences plus a few random ones."""
-    L = wl.seq_lens
-    pick = {int(np.argmax(L)), int(np.argmin(L))}
-    rng = np.random.default_rng(seed)
-    while len(pick) < min(n, len(L)):
-        pick.add(int(rng.integers(len(L))))
-    return sorted(pick)

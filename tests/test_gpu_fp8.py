@@ -12,7 +12,7 @@ import torch
 import oracle
 import paged_kv_cache_156_gb300 as pkv
 import workloads as W
-from gpu_harness import TOL, max_abs_err, sample_seqs, to_dev
+from gpu_harness import TOL, max_abs_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,7 @@ def test_full_size_fp8_workload():
     wl = W.build(W.SPECS["llama3_8b_fp8"], values="none")
     s = wl.spec
     dk, dv = W.device_pools(wl, 0, "cuda")
+    kc, vc = dk.cpu().numpy().copy(), dv.cpu().numpy().copy()     # the generator's pools, before the step
     ks, vs = wl.k_scales[0], wl.v_scales[0]
     pkv.paged_kv_append_fp8(to_dev(wl.k_new, s.dtype), to_dev(wl.v_new, s.dtype), dk, dv, cuda_of(wl.slot_mapping),
                             f32(ks), f32(vs))
@@ -102,12 +103,13 @@ def test_full_size_fp8_workload():
                                    max_seq_len=wl.max_seq_len)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
-    seqs = sample_seqs(wl, 5)
-    kc, vc = dk.cpu().numpy(), dv.cpu().numpy()
-    ref = oracle.attention_fp8_ref(wl.q[seqs], kc, vc, wl.block_tables[seqs], wl.seq_lens[seqs], wl.scale,
-                                   s.num_kv_heads, s.dtype, ks, vs)
-    err = max_abs_err(out, ref, seqs)
-    assert err <= TOL[s.dtype], f"max abs err {err} on sequences {seqs}"
+    oracle.append_fp8_ref(kc, vc, wl.k_new, wl.v_new, wl.slot_mapping, ks, vs, s.dtype)
+    assert np.array_equal(dk.cpu().numpy(), kc) and np.array_equal(dv.cpu().numpy(), vc)
+    ref = oracle.attention_fp8_ref(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype,
+                                   ks, vs)                 # every sequence, every head
+    err = max_abs_err(out, ref)
+    print(f"llama3_8b_fp8: max abs err {err:.3g} over all {s.num_seqs} sequences x {s.num_heads} heads")
+    assert err <= TOL[s.dtype], f"max abs err {err}"
 
 
 def test_copy_and_swap_fp8_pools_bit_exact():

@@ -1,11 +1,10 @@
 """GPU parity: the CUDA library against the CPU oracle, through the C ABI.
 
 Slot writes and block copies must match bit for bit; attention outputs within
-max-abs-error 2e-3 (fp16) / 1e-2 (bf16) of the float64 oracle.  Small and
-edge-case batches are compared element by element over every output; the
-full-size workloads, run in the launch configuration the benchmark times
-(automatic partition size), are compared on sampled sequences and checked
-whole for bit-exact cache state and finiteness.
+max-abs-error 2e-3 (fp16) / 1e-2 (bf16) of the float64 oracle.  Every batch,
+from the edge cases to the full-size workloads run in the launch
+configuration the benchmark times (automatic partition size), is compared
+element by element over every output and every cache element it checks.
 """
 import numpy as np
 import pytest
@@ -14,8 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_156_gb300 as pkv
 import workloads as W
-from gpu_harness import (TOL, DeviceStep, max_abs_err, oracle_attention, oracle_caches_after_step, sample_seqs,
-                         to_bits, to_dev)
+from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_attention, oracle_caches_after_step, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -207,10 +205,10 @@ def test_full_size_workload(name, mode):
     assert np.array_equal(to_bits(step.kc[0]), kc)
     assert np.array_equal(to_bits(step.vc[0]), vc)
     assert torch.isfinite(step.out[0]).all()
-    seqs = sample_seqs(wl, 6)
-    ref = oracle_attention(wl, kc, vc, seqs)
-    err = max_abs_err(step.out[0], ref, seqs)
-    assert err <= TOL[wl.spec.dtype], f"{name}: max abs err {err} on sequences {seqs}"
+    ref = oracle_attention(wl, kc, vc)              # every sequence, every head
+    err = max_abs_err(step.out[0], ref)
+    print(f"{name} ({mode}): max abs err {err:.3g} over all {s.num_seqs} sequences x {s.num_heads} heads")
+    assert err <= TOL[wl.spec.dtype], f"{name}: max abs err {err}"
 
 
 @pytest.mark.parametrize("mode", ["separate", "fused"])
@@ -223,12 +221,12 @@ def test_full_size_80_layer_step(mode):
     torch.cuda.synchronize()
     for l in range(80):
         assert torch.isfinite(step.out[l]).all(), f"layer {l}"
-    seqs = sample_seqs(wl, 3)
     for l in check_layers:
         kc, vc = oracle_caches_after_step(wl, *pre[l])
         assert np.array_equal(to_bits(step.kc[l]), kc) and np.array_equal(to_bits(step.vc[l]), vc)
-        ref = oracle_attention(wl, kc, vc, seqs)
-        err = max_abs_err(step.out[l], ref, seqs)
+        ref = oracle_attention(wl, kc, vc)          # all 16 sequences, every head
+        err = max_abs_err(step.out[l], ref)
+        print(f"llama2_70b_step ({mode}) layer {l}: max abs err {err:.3g} over all sequences x heads")
         assert err <= TOL[W.BF16], f"layer {l}: {err}"
 
 
