@@ -433,6 +433,9 @@ PKV_API pkv_status pkv_device_error(unsigned int* value, int reset);
  *     the counters a call needs zeroed are cleared on `stream` by the call
  *     itself.  Calls whose kernels overlap on the GPU (other streams, other
  *     host threads) race on the array: order them on one stream.
+ *   - The cached address belongs to the device's context at the first call.
+ *     After cudaDeviceReset (or any reset of the primary context) it is
+ *     stale: do not call this entry point again in that process.
  */
 #define PKV_STATIC_DECODE_SCRATCH_BYTES ((size_t)32 << 20)
 

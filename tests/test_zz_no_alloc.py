@@ -4,8 +4,12 @@ It serves callers that cannot call cudaMalloc (for example a plugin that a
 host engine gives only its input and output buffers), so its split-K scratch
 is an array built into the library.  These tests call it through the C ABI
 and compare its output with the regular entry point (which takes a caller
-workspace) on the same inputs, over consecutive calls with different batches,
-so later calls run on scratch that an earlier call left behind.
+workspace) on the same inputs: bit for bit, since both run the same kernels
+at the same partition size, and against the CPU oracle.  The calls come in a
+row with different batches, so every later call runs on scratch that an
+earlier call left behind: explicit split partitions, the automatic partition
+(the plan kernel zeroes the merge counters in the array), and a batch of
+more sequences than the plan lists (the counters are cleared by a memset).
 
 The file name makes pytest collect it last: a run that stops at the first
 failure has already run every other test.  It builds and loads the library
@@ -17,7 +21,7 @@ import torch
 
 import paged_kv_cache_156_gb300 as pkv
 import workloads as W
-from gpu_harness import TOL, DeviceStep
+from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_attention, oracle_caches_after_step
 from paged_kv_cache_156_gb300 import _build
 
 pytestmark = pytest.mark.gpu
@@ -42,29 +46,41 @@ def decode_static(lib, step, partition_tokens):
     return out
 
 
-CASES = [
-    (W.small_spec(num_seqs=5, num_heads=32, num_kv_heads=8, dtype=W.BF16, seed=31,
-                  lens=("fixed", (3000, 700, 64, 65, 1500))), 256),
-    (W.small_spec(num_seqs=4, num_heads=16, num_kv_heads=2, dtype=W.F16, block_size=32, seed=32,
-                  lens=("fixed", (2049, 1, 513, 4000))), 512),
-]
+CASES = {
+    # split partitions at an explicit size
+    "A": (W.small_spec(num_seqs=5, num_heads=32, num_kv_heads=8, dtype=W.BF16, seed=31,
+                       lens=("fixed", (3000, 700, 64, 65, 1500))), 256),
+    "B": (W.small_spec(num_seqs=4, num_heads=16, num_kv_heads=2, dtype=W.F16, block_size=32, seed=32,
+                       lens=("fixed", (2049, 1, 513, 4000))), 512),
+    # automatic partition size: the plan kernel picks it and zeroes the counters
+    "C": (W.small_spec(num_seqs=7, num_heads=32, num_kv_heads=8, dtype=W.BF16, seed=33,
+                       lens=("fixed", (5000, 1, 2100, 64, 3333, 700, 129))), 0),
+    # more sequences than the plan lists: the full grid, counters cleared by a memset
+    "D": (W.small_spec(num_seqs=pkv.PLAN_MAX_SEQS + 77, num_heads=8, num_kv_heads=2, head_dim=64, seed=34,
+                       lens=("uniform", 0, 150), pool=("headroom", 0.1)), 64),
+}
 
 
 def test_static_decode_matches_workspace_decode_on_consecutive_calls(lib):
-    steps = []
-    for spec, p in CASES:
-        step = DeviceStep(W.build(spec), partition_tokens=p)
+    steps = {}
+    for name, (spec, p) in CASES.items():
+        wl = W.build(spec)
+        step = DeviceStep(wl, partition_tokens=p)
         pkv.paged_kv_append(step.k_new, step.v_new, step.kc[0], step.vc[0], step.slot_mapping)
         step.decode(0)                              # regular entry point, caller workspace
-        steps.append((step, p))
-    # three calls in a row on the shared scratch: batch A, batch B, batch A again
-    for step, p in (steps[0], steps[1], steps[0]):
+        kc, vc = oracle_caches_after_step(wl, wl.key_caches[0], wl.value_caches[0])
+        steps[name] = (step, p, oracle_attention(wl, kc, vc))
+    torch.cuda.synchronize()
+    # calls in a row on the shared scratch, each after a different batch left its contents
+    for name in ("A", "B", "A", "C", "D", "A", "C"):
+        step, p, ref = steps[name]
         got = decode_static(lib, step, p)
         torch.cuda.synchronize()
-        ref = step.out[0].float()
-        err = float((got.float() - ref).abs().max())
         assert torch.isfinite(got).all()
-        assert err <= TOL[step.wl.spec.dtype], f"static-scratch decode differs from workspace decode by {err}"
+        assert torch.equal(got.view(torch.int16), step.out[0].view(torch.int16)), \
+            f"batch {name}: static-scratch decode differs from the workspace decode"
+        err = max_abs_err(got, ref)
+        assert err <= TOL[step.wl.spec.dtype], f"batch {name}: max abs err {err} against the oracle"
     assert pkv.device_error(reset=True) == 0
 
 
