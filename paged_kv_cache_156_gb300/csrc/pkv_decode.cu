@@ -45,8 +45,7 @@
 //        M = max_p m_p,  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
 //  * Every wait is an mbarrier wait bounded in wall time; a wait that gives
 //    up raises the error word and the CTA winds down.
-#include <stdlib.h>
-
+#include <atomic>
 #include <type_traits>
 
 #include "pkv_decode_common.cuh"
@@ -405,56 +404,26 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensor
     return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
 }
 
-int fp8_stages();
+// Pipeline shapes (one per pool type, measured best on the 8B-shaped, 70B
+// mixed and 80-layer batches): 16-bit pools run 4 consumer warps over 64-position
+// chunks with a 2-stage ring, three CTAs per SM at head_dim 128; E4M3 pools the
+// same chunks with 4 stages (the same ring bytes); the multi-query form
+// likewise.
+constexpr int kCW = 4;             // consumer warps
+constexpr int kStages16 = 2;       // ring depth over 16-bit pools
+constexpr int kStages8 = 4;        // and over E4M3 pools
 
 template <typename T, int D>
-cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int warps, int stages,
-                       cudaStream_t s) {
-    if (a.num_queries > 1) {                        // verify: one shape per pool type
-        if constexpr (D == 128)
-            if (a.kv8) return launch_t<T, D, 4, 4, true, true>(a, tmk, tmv, s);
-        if (a.kv8) return cudaErrorInvalidValue;
-        return launch_t<T, D, 4, 2, true>(a, tmk, tmv, s);
-    }
-    if (a.kv8) {                                    // E4M3 pools: stages of 64 positions (8 KB each of K, V)
+cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
+    if (a.kv8) {
         if constexpr (D == 128) {
-            switch (fp8_stages()) {
-                case 2: return launch_t<T, D, 4, 2, false, true>(a, tmk, tmv, s);
-                case 3: return launch_t<T, D, 4, 3, false, true>(a, tmk, tmv, s);
-                default: return launch_t<T, D, 4, 4, false, true>(a, tmk, tmv, s);
-            }
+            if (a.num_queries > 1) return launch_t<T, D, kCW, kStages8, true, true>(a, tmk, tmv, s);
+            return launch_t<T, D, kCW, kStages8, false, true>(a, tmk, tmv, s);
         }
         return cudaErrorInvalidValue;
     }
-    if (warps == 2) {
-        switch (stages) {
-            case 2: return launch_t<T, D, 2, 2>(a, tmk, tmv, s);
-            case 4: return launch_t<T, D, 2, 4>(a, tmk, tmv, s);
-            default: return launch_t<T, D, 2, 3>(a, tmk, tmv, s);
-        }
-    }
-    switch (stages) {
-        case 3: return launch_t<T, D, 4, 3>(a, tmk, tmv, s);
-        case 4: return launch_t<T, D, 4, 4>(a, tmk, tmv, s);
-        default: return launch_t<T, D, 4, 2>(a, tmk, tmv, s);
-    }
-}
-
-// Pipeline shape: 4 consumer warps (64-position chunks) with a 2-stage ring,
-// three CTAs per SM at head_dim 128.  PKV_DECODE_WARPS in {2, 4} and
-// PKV_DECODE_STAGES in {2, 3, 4} override it (tuning knobs; read once).
-int env_choice(const char* name, int dflt, int lo, int hi) {
-    const char* e = getenv(name);
-    const int x = e ? atoi(e) : dflt;
-    return (x >= lo && x <= hi) ? x : dflt;
-}
-int ring_stages() {
-    static const int v = env_choice("PKV_DECODE_STAGES", 2, 2, 4);
-    return v;
-}
-int consumer_warps() {
-    static const int v = env_choice("PKV_DECODE_WARPS", 4, 2, 4) == 2 ? 2 : 4;
-    return v;
+    if (a.num_queries > 1) return launch_t<T, D, kCW, kStages16, true>(a, tmk, tmv, s);
+    return launch_t<T, D, kCW, kStages16>(a, tmk, tmv, s);
 }
 
 }  // namespace
@@ -485,34 +454,20 @@ int occupancy_of() {
     return n;
 }
 
-template <int D>
-int occupancy_cfg(int cw, int st) {
-    if (cw == 2) return st == 2 ? occupancy_of<__half, D, 2, 2>() : st == 4 ? occupancy_of<__half, D, 2, 4>()
-                                                                           : occupancy_of<__half, D, 2, 3>();
-    return st == 3 ? occupancy_of<__half, D, 4, 3>() : st == 4 ? occupancy_of<__half, D, 4, 4>()
-                                                               : occupancy_of<__half, D, 4, 2>();
-}
-
-// E4M3 pools: 4 stages unless PKV_DECODE_STAGES says otherwise
-int fp8_stages() {
-    static const int v = env_choice("PKV_DECODE_STAGES", 4, 2, 4);
-    return v;
-}
-
-int occupancy_fp8() {
-    const int st = fp8_stages();
-    return st == 2 ? occupancy_of<__half, 128, 4, 2, true>() : st == 3 ? occupancy_of<__half, 128, 4, 3, true>()
-                                                                       : occupancy_of<__half, 128, 4, 4, true>();
-}
 }  // namespace
 
 int decode_ctas_per_sm(int head_dim, bool kv8) {
-    static int cache[3] = {-1, -1, -1};           // head_dim 64, 128, E4M3; the same on every GB300
+    // head_dim 64, 128, E4M3; the same on every GB300, so host threads that race
+    // on a first call store the same value
+    static std::atomic<int> cache[3] = {-1, -1, -1};
     const int i = kv8 ? 2 : head_dim == 64 ? 0 : 1;
-    if (cache[i] < 0) cache[i] = kv8 ? occupancy_fp8()
-                                     : i == 0 ? occupancy_cfg<64>(consumer_warps(), ring_stages())
-                                              : occupancy_cfg<128>(consumer_warps(), ring_stages());
-    return cache[i];
+    int n = cache[i].load(std::memory_order_relaxed);
+    if (n < 0) {
+        n = kv8 ? occupancy_of<__half, 128, kCW, kStages8, true>()
+                : i == 0 ? occupancy_of<__half, 64, kCW, kStages16>() : occupancy_of<__half, 128, kCW, kStages16>();
+        cache[i].store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
@@ -529,13 +484,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
         e = cudaMemsetAsync(a.tickets, 0, n, s);
     }
     if (e != cudaSuccess) return e;
-    const int st = ring_stages(), cw = consumer_warps();
-    if (dtype == 0) {
-        return head_dim == 128 ? launch_cfg<__half, 128>(a, tmk, tmv, cw, st, s)
-                               : launch_cfg<__half, 64>(a, tmk, tmv, cw, st, s);
-    }
-    return head_dim == 128 ? launch_cfg<__nv_bfloat16, 128>(a, tmk, tmv, cw, st, s)
-                           : launch_cfg<__nv_bfloat16, 64>(a, tmk, tmv, cw, st, s);
+    if (dtype == 0)
+        return head_dim == 128 ? launch_cfg<__half, 128>(a, tmk, tmv, s) : launch_cfg<__half, 64>(a, tmk, tmv, s);
+    return head_dim == 128 ? launch_cfg<__nv_bfloat16, 128>(a, tmk, tmv, s)
+                           : launch_cfg<__nv_bfloat16, 64>(a, tmk, tmv, s);
 }
 
 }  // namespace pkv

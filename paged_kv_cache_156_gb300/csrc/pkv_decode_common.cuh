@@ -14,7 +14,6 @@ namespace dec {
 
 constexpr int kMaxTable = kPlanTableEntries;   // staged table entries: part_tokens (<= 4096) / block_size (>= 8)
 constexpr int kHeadsPerCta = 8;      // mma N: query heads served by one CTA
-constexpr int kMaxParts = 512;       // partitions per sequence the in-kernel merge handles
 
 // CW consumer warps each own 16 positions of a chunk of 16 * CW positions;
 // EB is the pool's element size (2: fp16 / bf16; 1: E4M3 codes).

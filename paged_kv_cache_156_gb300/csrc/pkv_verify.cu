@@ -22,8 +22,6 @@
 // merges lane by lane through shared memory after the last chunk.  Split
 // partitions merge through the workspace with the same ticket protocol as
 // decode (the last partition merges).
-#include <stdlib.h>
-
 #include <atomic>
 
 #include "pkv_decode_common.cuh"
@@ -550,12 +548,9 @@ cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
 namespace pkv {
 
 int verify_rows_per_cta(int rows) {
-    static const int forced = [] {
-        const char* e = getenv("PKV_VERIFY_ROWS");       // tuning knob: 32 or 64 rows per CTA
-        return e ? atoi(e) : 0;
-    }();
-    if (rows <= kVRows / 2) return kVRows / 2;
-    return forced == kVRows / 2 ? kVRows / 2 : kVRows;
+    // up to 32 rows: two warps per 16-row tile; more: 64-row CTAs (two 32-row
+    // CTAs per KV head measured slower: their K/V bytes leave HBM twice)
+    return rows <= kVRows / 2 ? kVRows / 2 : kVRows;
 }
 
 int verify_ctas_per_sm(int head_dim, int rows) {
