@@ -452,15 +452,27 @@ class BlockEngineRef:
         del self.lens[seq_id]
         return True
 
-    def _needs_block(self, s):
-        L = self.lens[s]
-        return L % self.bs == 0 or self.ref[self.tables[s][-1]] > 1
+    def _blocks_needed(self, seq_ids):
+        """Free blocks the call takes: one per sequence whose last block is full,
+        and one per copy-on-write.  A shared block is copied by each writer only
+        while another sequence still holds it (P1 §4.2.2), so of its r holders,
+        k of them writing in this call, min(k, r - 1) copy it and the last holder
+        writes in place."""
+        full = 0
+        writers = {}
+        for s in seq_ids:
+            last = self.tables[s][-1] if self.tables[s] else None
+            if self.lens[s] % self.bs == 0:
+                full += 1
+            elif self.ref[last] > 1:
+                writers[last] = writers.get(last, 0) + 1
+        return full + sum(min(k, self.ref[b] - 1) for b, k in writers.items())
 
     def append_slots(self, seq_ids):
         """One token for each sequence; (slots, copy-on-write pairs) or None."""
         if len(set(seq_ids)) != len(seq_ids) or any(s not in self.tables for s in seq_ids):
             return None
-        if sum(self._needs_block(s) for s in seq_ids) > len(self.free_list):
+        if self._blocks_needed(seq_ids) > len(self.free_list):
             return None
         slots, pairs = [], []
         for s in seq_ids:

@@ -15,6 +15,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <deque>
 #include <new>
 #include <unordered_map>
@@ -136,6 +137,7 @@ pkv_status pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, in
     const int bs = bm->block_size;
     // check first, change nothing unless every sequence can take its token
     std::unordered_set<int64_t> seen;
+    std::unordered_map<int32_t, int64_t> writers;               // shared partly filled last block -> listed holders
     int64_t need_blocks = 0, need_cow = 0;
     for (int64_t i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
@@ -145,9 +147,16 @@ pkv_status pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, in
         if (sq.num_tokens % bs == 0) {
             ++need_blocks;                                       // the last block is full (or none yet)
         } else if (bm->refcount[sq.blocks.back()] > 1) {
-            ++need_blocks;                                       // shared partly filled block: copy on write
-            ++need_cow;
+            ++writers[sq.blocks.back()];
         }
+    }
+    // A shared partly filled block with r holders, k of them listed: each listed
+    // holder copies it while another sequence still holds it, so the last of all
+    // r holders writes in place: min(k, r - 1) copies.
+    for (const auto& w : writers) {
+        const int64_t copies = std::min<int64_t>(w.second, bm->refcount[w.first] - 1);
+        need_blocks += copies;
+        need_cow += copies;
     }
     if (need_cow > 0 && (!cow_pairs || cow_capacity < need_cow))
         return err(PKV_ERR_INVALID, "append_slots: cow_pairs buffer too small");

@@ -78,6 +78,33 @@ def test_fork_shares_then_copies_on_write():
     assert bm.num_free_blocks == 16
 
 
+def test_last_holder_of_a_shared_block_needs_no_free_block():
+    """Two forks share a partly filled block and both append with one block free:
+    the first copies it, the second (now its only holder) writes in place, so the
+    call fits (P1 §4.2.2: a block is copied only while another sequence holds it)."""
+    for make in (lambda: pkv.BlockManager(3, 8), lambda: oracle.BlockEngineRef(3, 8)):
+        bm = make()
+        bm.allocate(0, 12)                   # blocks 0, 1; block 1 holds 4 tokens
+        bm.fork(0, 1)
+        bm.allocate(2, 1)                    # block 2: the pool is now empty
+        bm.free(2)                           # one free block
+        got = bm.append_slots([0, 1])
+        assert got is not None
+        slots, cow = got
+        assert [tuple(int(x) for x in p) for p in cow] == [(1, 2)]
+        assert [int(x) for x in slots] == [2 * 8 + 4, 1 * 8 + 4]
+    # three holders, two of them writing: both copy (a third sequence still holds the block)
+    bm = pkv.BlockManager(4, 8)
+    ref = oracle.BlockEngineRef(4, 8)
+    for m in (bm, ref):
+        m.allocate(0, 12)
+        m.fork(0, 1)
+        m.fork(0, 2)
+    slots, cow = bm.append_slots([0, 1])
+    want = ref.append_slots([0, 1])
+    assert cow.tolist() == [[1, 2], [1, 3]] and [tuple(p) for p in want[1]] == [(1, 2), (1, 3)]
+
+
 def test_fork_at_block_boundary_needs_no_copy():
     bm = pkv.BlockManager(8, 16)
     bm.allocate(0, 32)
