@@ -40,6 +40,7 @@ import workloads as W  # noqa: E402
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0       # GB300 HBM3e nominal bandwidth: context beside the measured peak
+MIN_DECODE_EVENTS = 50         # CUDA-event samples behind the decode launch's median
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak); decode tokens/s"
 
 
@@ -411,8 +412,14 @@ def run_pkv(args, rank, world, local):
     t1.record()
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
+    # the decode launch's median needs at least MIN_DECODE_EVENTS samples: steps
+    # past the timed region (not in `value`) add events when K is smaller
+    n_timed_events = len(ev_pairs)
+    for i in range(max(0, MIN_DECODE_EVENTS - n_timed_events)):
+        step(args.steps + i, True)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
     max_ms = max_over_ranks(elapsed_ms, world)
     dec_launches = spec.num_layers - 1 if (fused and spec.num_layers > 1) else 1
     dec_ms = float(np.median([a.elapsed_time(b) for a, b in ev_pairs])) / dec_launches
@@ -426,8 +433,7 @@ def run_pkv(args, rank, world, local):
     traffic = profiled_traffic(args.workload)
 
     # ---- end to end: inputs from pinned host memory, outputs read back, every step
-    e2e = None
-    if not args.no_e2e:
+    def measure_e2e(use_graph):
         host_in = [t.cpu().pin_memory() for t in (q, k_new, v_new, slots, tables, lens)]
         dev_in = [q, k_new, v_new, slots, tables, lens]
         # two pinned output buffers: the host reads step i-1's outputs while the GPU runs step i
@@ -449,7 +455,7 @@ def run_pkv(args, rank, world, local):
                 h.copy_(o, non_blocking=True)
 
         graphs = None
-        if not args.e2e_eager:
+        if use_graph:
             # one CUDA graph per (pool replica, output buffer), captured through the same
             # public calls; a replay copies the inputs in, plans, decodes and copies the
             # outputs back, with one launch from the host
@@ -470,6 +476,9 @@ def run_pkv(args, rank, world, local):
                     graphs[(r, j)] = g
             torch.cuda.synchronize()
             assert pkv.device_error() == 0, "device error word raised while capturing"
+        else:
+            for i in range(3):                   # warm the eager path's host side
+                whole_step(i, i % 2)
 
         torch.cuda.synchronize()
         barrier(world)
@@ -487,14 +496,22 @@ def run_pkv(args, rank, world, local):
         done[(n_e2e - 1) % 2].synchronize()
         seen += read_result(host_out[(n_e2e - 1) % 2])
         e2e_s = max_over_ranks(time.perf_counter() - w0, world)
-        e2e = {"value": round(world * nbytes["step"] * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
-               "ms_per_step": round(e2e_s * 1e3 / n_e2e, 4),
-               "pipeline": ("every step copies its inputs in from pinned memory and its outputs back; the host "
-                            "reads step i's outputs while the GPU runs step i+1; " +
-                            ("each step is one replay of a CUDA graph of the public calls"
-                             if graphs is not None else "every call issued from Python")),
-               "finite": bool(math.isfinite(seen))}
+        return {"value": round(world * nbytes["step"] * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+                "ms_per_step": round(e2e_s * 1e3 / n_e2e, 4),
+                "pipeline": ("every step copies its inputs in from pinned memory and its outputs back; the host "
+                             "reads step i's outputs while the GPU runs step i+1; " +
+                             ("each step is one replay of a CUDA graph of the public calls"
+                              if graphs is not None else
+                              "every call issued from Python through the C ABI (host validation and "
+                              "launch set-up on every step)")),
+                "finite": bool(math.isfinite(seen))}
+
+    e2e = e2e_eager = None
+    if not args.no_e2e:
+        e2e = measure_e2e(not args.e2e_eager)
+        if not args.e2e_eager:
+            e2e_eager = measure_e2e(False)
 
     # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
     cpu = None
@@ -550,9 +567,11 @@ def run_pkv(args, rank, world, local):
                      "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(dec_gbs / NOMINAL_HBM_GBS, 4),
-                     "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 5)},
+                     "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 5),
+                     "launch_events": len(ev_pairs), "launch_events_in_timed_region": n_timed_events},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_eager": e2e_eager,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
