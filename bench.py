@@ -73,6 +73,8 @@ def parse_args():
                    help="run a multi-layer workload with this many layers (same per-layer shape; 0 = all)")
     p.add_argument("--separate-append", action="store_true",
                    help="launch paged_kv_append and the decode separately instead of the fused call")
+    p.add_argument("--replicas", type=int, default=0,
+                   help="pool replicas rotated between steps (0: enough to exceed L2; 1 for small profiler captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -322,6 +324,8 @@ def run_pkv(args, rank, world, local):
     replicas = max(2, min(4, math.ceil(3 * L2_BYTES / footprint))) if spec.num_layers == 1 else 1
     if footprint * replicas > 0.6 * torch.cuda.get_device_properties(dev).total_memory:
         replicas = 1
+    if args.replicas > 0:
+        replicas = args.replicas
     pools = []
     for r in range(replicas):
         kcs, vcs = [], []

@@ -166,6 +166,14 @@ PKV_API int pkv_decode_plan_partition_tokens(const void* workspace, int num_seqs
  *                 1.4 times, multiples of 512, at least
  *                 pkv_decode_partition_tokens); the output does not depend
  *                 on that order.
+ *   Shared prefixes: the plan compares the block-table rows of adjacent
+ *   sequences whose first entries agree (forks of one prompt, P2 §3.3) and,
+ *   with at most 4 query heads per KV head and 16-bit pools, serves up to
+ *   8 / (num_heads / num_kv_heads) sequences that share at least 256 leading
+ *   positions in one CTA per KV head: the shared blocks are streamed once for
+ *   all of them, then each sequence's own blocks, each sequence's heads
+ *   seeing the shared positions and its own.  The result is that of the
+ *   sequences attended one by one, up to the summation order.
  * head_dim in {64, 128}; block_size in {8, 16, 32}; num_heads a multiple of
  * num_kv_heads.
  */

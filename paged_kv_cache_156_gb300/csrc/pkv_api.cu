@@ -183,8 +183,17 @@ int resolve_partition(int num_seqs, int num_heads, int num_kv_heads, int max_seq
                             pkv::decode_ctas_per_sm(head_dim));
 }
 
+// Partials per query row the workspace holds: the longest sequence's
+// partitions at the smallest partition size, plus one when the plan may form
+// shared-prefix units (at most 4 query rows per KV head): a unit's stream runs
+// past the longest member by the other members' own segments.
+int64_t partial_slots(int max_seq_len, int part, int rows_per_kv_head) {
+    const int64_t base = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
+    return base + (rows_per_kv_head <= pkv::dec_heads_per_cta() / 2 ? 1 : 0);
+}
+
 size_t workspace_for(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_seq_len, int part) {
-    const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
+    const int64_t max_parts = partial_slots(max_seq_len, part, num_heads / num_kv_heads);
     return pkv::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, static_cast<int>(max_parts))
         .total();
 }
@@ -326,10 +335,11 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
 
     const int dev = current_device();
     const int part = resolve_partition(num_seqs, rows, num_kv_heads, max_seq_len, partition_tokens, head_dim);
-    const int64_t max_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
-    if (max_parts > 512)
+    const int64_t base_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
+    if (base_parts > 512)
         return fail(PKV_ERR_UNSUPPORTED, "%lld partitions per sequence (at most 512; use a larger partition_tokens)",
-                    static_cast<long long>(max_parts));
+                    static_cast<long long>(base_parts));
+    const int64_t max_parts = partial_slots(max_seq_len, part, rows / num_kv_heads);
     const pkv::DecodeWorkspace lay =
         pkv::decode_workspace_layout(num_seqs, rows, num_kv_heads, head_dim, static_cast<int>(max_parts));
     const size_t need = lay.total();
@@ -380,6 +390,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
                                                 : pkv::decode_ctas_per_sm(head_dim, kv8));
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
+    a.direct_parts = static_cast<int>(base_parts);
     // work-list entries the grid covers: every (sequence, partition) the longest sequence
     // could need, or, with the lengths' sum known, at most B + sum / P entries (a sequence
     // of length l has max(1, ceil(l / P)) <= 1 + l / P partitions)
@@ -400,6 +411,10 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     }
     a.plan_capacity = static_cast<int>(capacity);
     a.sum_seq_lens = sum_seq_lens;
+    // shared-prefix units: one query token over 16-bit pools, the members' query heads in one
+    // CTA's columns.  (A unit's stream is never longer than its members' lengths' sum, since it
+    // shares at least kUnitMinShare positions, so the grid bound above still holds.)
+    a.units = num_queries == 1 && !kv8 && a.qgroup <= pkv::dec_heads_per_cta() / 2;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.kv8 = kv8;
     a.k_scale = k_scale;

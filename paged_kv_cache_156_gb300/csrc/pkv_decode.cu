@@ -58,14 +58,16 @@ using dec::Geo;
 using dec::kHeadsPerCta;
 using dec::kMaxTable;
 
-template <int D, int CW, int STAGES, int EB = 2>
+template <int D, int CW, int STAGES, int EB = 2, bool UNITS = false>
 struct Smem {
     using G = Geo<D, CW, EB>;
     static constexpr size_t kRing = 2 * STAGES * G::kStage;
     static constexpr size_t kArena = kRing > size_t(G::kScratch) ? kRing : size_t(G::kScratch);  // scratch aliases the ring
     static constexpr size_t kBars = kArena;
     static constexpr size_t kTable = kBars + (2 * STAGES + 1) * sizeof(uint64_t);
-    static constexpr size_t kMisc = kTable + kMaxTable * sizeof(int);
+    static constexpr size_t kDesc = kTable + kMaxTable * sizeof(int);   // shared-prefix unit: per staged block
+    static constexpr size_t kUnit = kDesc + (UNITS ? kMaxTable : 0) * sizeof(int);   // unit layout
+    static constexpr size_t kMisc = kUnit + (UNITS ? 2 * kHeadsPerCta + 2 : 0) * sizeof(int);
     static constexpr size_t kBytes = kMisc + 16;
 };
 
@@ -80,14 +82,17 @@ __device__ __forceinline__ uint32_t q_as_f16x2<__nv_bfloat16>(uint32_t x) {
 }
 
 // KV8: the pools hold E4M3 codes (head_dim 128); the tensor cores run in f16.
-template <typename T, int D, int CW, int STAGES, bool MQ, bool KV8 = false>
+// UNITS: the work list may hold shared-prefix units (16-bit decode only; the
+// host launches this form when the plan may make them).
+template <typename T, int D, int CW, int STAGES, bool MQ, bool KV8 = false, bool UNITS = false>
 __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                      const __grid_constant__ CUtensorMap tmv,
                                                                      const DecodeArgs a) {
     static_assert(!KV8 || D == 128, "E4M3 pools: head_dim 128");
     constexpr int kEB = KV8 ? 1 : 2;                // bytes of a pool element
+    constexpr bool kUnits = UNITS && !MQ && !KV8;   // shared-prefix units: 16-bit decode
     using G = Geo<D, CW, kEB>;
-    using S = Smem<D, CW, STAGES, kEB>;
+    using S = Smem<D, CW, STAGES, kEB, kUnits>;
     constexpr int kChunk = G::kChunk;
     constexpr int kConsumers = G::kConsumers;
     constexpr int kThreads = G::kThreads;
@@ -98,28 +103,47 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     uint64_t* empty = full + STAGES;
     uint64_t* epi = empty + STAGES;               // consumer-group barrier (all consumer threads)
     int* tbl = reinterpret_cast<int*>(smem + S::kTable);
+    // a unit's staged blocks: segment + 1 (0: the shared prefix) | first valid offset << 8 | end offset << 16
+    int* udesc = reinterpret_cast<int*>(smem + S::kDesc);
+    int* useg = reinterpret_cast<int*>(smem + S::kUnit);   // members' first stream blocks; [members]: the total
+    int* ulen = useg + kHeadsPerCta + 1;                   // members' lengths; [kHeadsPerCta]: layout refused
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kMisc);
     volatile int* merge_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     grid_dependency_wait();                         // the plan and the pools come from earlier kernels
-    // Work item: from the plan (one entry per (sequence, partition), KV head
+    // Work item: from the plan (one entry per (unit, partition), KV head
     // groups innermost in the 1-D grid) or, without one, the 3-D grid itself.
+    // A unit is one sequence, or (16-bit decode) `un` adjacent sequences that
+    // share their first `ush` positions, whose stream is Lp positions long.
     int hh, part, s, P, Lp;
+    int un = 1, ush = 0, ul0 = 0, ul1 = 0;          // (units: the first two members' lengths)
     if (a.plan) {
         const int nh = a.num_kv_heads * a.head_groups;
         const unsigned y = blockIdx.x / static_cast<unsigned>(nh);
         hh = static_cast<int>(blockIdx.x - y * static_cast<unsigned>(nh));
-        const int4 it = __ldg(a.plan + y);
+        const int4 it = __ldg(a.plan + kPlanEntryInts * y);
+        const int4 iu = __ldg(a.plan + kPlanEntryInts * y + 1);
         s = it.x;
         part = it.y;
         Lp = it.z;
         P = it.w;
+        un = iu.x;
+        ush = iu.y;
+        ul0 = iu.z;
+        ul1 = iu.w;
         if (s < 0) return;                          // padding entry
         // a plan made for other batch arguments (a run-only call's misuse): never index out of range
-        if (s >= a.num_seqs || part < 0 || Lp < 0 || Lp > a.max_seq_len || P < 64 || P > kMaxTable * a.block_size ||
-            part * P >= max(Lp, 1) || (Lp + P - 1) / P > a.max_parts) {
+        bool bad = s >= a.num_seqs || part < 0 || Lp < 0 || P < 64 || P > kMaxTable * a.block_size ||
+                   part * P >= max(Lp, 1) || (Lp + P - 1) / P > a.max_parts || un < 1;
+        if (un == 1)
+            bad = bad || Lp > a.max_seq_len;
+        else
+            bad = bad || !kUnits || un * a.group > kHeadsPerCta || a.head_groups != 1 || s + un > a.num_seqs ||
+                  ush < 1 || ush > a.max_seq_len || Lp % a.block_size != 0 ||
+                  static_cast<int64_t>(Lp) > static_cast<int64_t>(un) * (a.max_seq_len + a.block_size);
+        if (bad) {
             if (threadIdx.x == 0) raise_error(a.err, kErrBounds);
             return;
         }
@@ -130,11 +154,14 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         P = a.part_tokens;
         Lp = -1;
     }
+    const bool grouped = kUnits && un > 1;          // a shared-prefix unit (CTA-uniform)
     const int hg = hh % a.head_groups;
     const int kvh = hh / a.head_groups;
     const int vh0 = hg * kHeadsPerCta;                // first query row of this CTA within the KV head's rows
-    const int gc = min(kHeadsPerCta, a.group - vh0);
+    // columns: the rows of this CTA (a unit's column c is head c % group of member c / group)
+    const int gc = grouped ? un * a.group : min(kHeadsPerCta, a.group - vh0);
     const int64_t sh0 = dec::item_row0<MQ>(a, s, kvh, vh0);
+    const dec::ItemRows rows{sh0, s, kvh, vh0, grouped ? un : 1};
     const int bs = a.block_size;
     const int start = part * P;
     T* out = reinterpret_cast<T*>(a.out);
@@ -153,20 +180,22 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     uint4 nrow = make_uint4(0u, 0u, 0u, 0u);
     int64_t nslot = -1;
     float nscale = 1.0f;
-    const bool maybe_put = !MQ && a.k_new != nullptr && (Lp <= 0 || part == (Lp + P - 1) / P - 1);
+    const bool maybe_put = !MQ && !grouped && a.k_new != nullptr && (Lp <= 0 || part == (Lp + P - 1) / P - 1);
     if (warp == CW) {
-        const int32_t* row = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + first_blk;
+        if (!grouped) {                             // (a unit's blocks are staged once its lengths are known)
+            const int32_t* row = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + first_blk;
 #pragma unroll
-        for (int k = 0; k < kTePerLane; ++k) {
-            const int i = lane + 32 * k;
-            te[k] = (32 * k < tcount && i < tcount) ? __ldg(row + i) : 0;
-        }
-        if (maybe_put) {
-            nslot = __ldg(a.slot_mapping + s);
-            if (lane < 2 * kHV) {
-                const uint4* src = lane < kHV ? a.k_new : a.v_new;
-                nrow = __ldg(src + (static_cast<int64_t>(s) * a.num_kv_heads + kvh) * kHV + lane % kHV);
-                if constexpr (KV8) nscale = __ldg((lane < kHV ? a.k_scale : a.v_scale) + kvh);
+            for (int k = 0; k < kTePerLane; ++k) {
+                const int i = lane + 32 * k;
+                te[k] = (32 * k < tcount && i < tcount) ? __ldg(row + i) : 0;
+            }
+            if (maybe_put) {
+                nslot = __ldg(a.slot_mapping + s);
+                if (lane < 2 * kHV) {
+                    const uint4* src = lane < kHV ? a.k_new : a.v_new;
+                    nrow = __ldg(src + (static_cast<int64_t>(s) * a.num_kv_heads + kvh) * kHV + lane % kHV);
+                    if constexpr (KV8) nscale = __ldg((lane < kHV ? a.k_scale : a.v_scale) + kvh);
+                }
             }
         }
     } else if constexpr (KV8) {
@@ -188,7 +217,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         const int kq = (lane & 3) * 2;
         const int nq = min(n, gc - 1);      // lanes of absent rows read a present row, then drop it
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(a.q) +
-                                                                 dec::qo_row<MQ>(a, sh0, s, kvh, vh0, nq) * D);
+                                                                 rows.out<MQ>(a, nq) * D);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             ws.qb[ks][0] = n < gc ? __ldg(qrow + (ks * 16 + kq) / 2) : 0u;
@@ -216,6 +245,116 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     const int end = min(L, start + P);
     const int nparts = (L + P - 1) / P;
     const int nchunks = (end - start + kChunk - 1) / kChunk;
+    const int lbs = 31 - __clz(bs);                 // block sizes are powers of two
+    const int sb0 = start >> lbs;                   // a unit's first stream block of this partition
+    const int nblk = (end - start + bs - 1) >> lbs;
+    // a unit's fused slot writes: member `lane`'s slot, and the new rows of its first
+    // two members (lanes < 2 * D / 8), loaded with its lengths (they depend on nothing else)
+    constexpr int kUnitRows = 2;
+    int64_t uslot = -1;
+    uint4 urow[kUnitRows];
+#pragma unroll
+    for (int j = 0; j < kUnitRows; ++j) urow[j] = make_uint4(0u, 0u, 0u, 0u);
+
+    if (grouped && warp == CW) {
+        if (a.k_new != nullptr) {
+            if (lane < un) uslot = __ldg(a.slot_mapping + s + lane);
+            if (lane < 2 * kHV) {
+                const uint4* src = lane < kHV ? a.k_new : a.v_new;
+#pragma unroll
+                for (int j = 0; j < kUnitRows; ++j)
+                    if (j < un) urow[j] = __ldg(src + (static_cast<int64_t>(s + j) * a.num_kv_heads + kvh) * kHV + lane % kHV);
+            }
+        }
+        // The unit's stream: the shared prefix (blocks [0, nsb) of the first member,
+        // positions < ush), then each member j whose length exceeds ush: its blocks
+        // from fb = ush / bs on, positions [ush, L_j).  Staged here (before the CTA
+        // barrier, so every warp sees it): each block of this partition with its
+        // physical id, its segment and the valid offsets within it.
+        const int fb = ush >> lbs, nsb = (ush + bs - 1) >> lbs;
+        // member lengths: the first two come with the work item
+        int Lj = lane == 0 ? ul0 : lane == 1 ? ul1 : 0;
+        if (lane >= 2 && lane < un) Lj = __ldg(a.seq_lens + s + lane);
+        Lj = lane < un ? min(max(Lj, 0), a.max_seq_len) : 0;
+        const int cnt = (lane < un && Lj > ush) ? ((Lj + bs - 1) >> lbs) - fb : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const int total = nsb + __shfl_sync(0xffffffffu, incl, 31);
+        // the plan's stream must be this one: lengths changed since the plan otherwise
+        const bool layout_ok = (static_cast<int64_t>(total) << lbs) == Lp;
+        if (lane < un) {
+            useg[lane] = nsb + incl - cnt;
+            ulen[lane] = Lj;
+        }
+        if (lane == 0) {
+            useg[un] = total;
+            ulen[kHeadsPerCta] = !layout_ok;
+            if (!layout_ok) raise_error(a.err, kErrBounds);
+        }
+        __syncwarp();
+        for (int i = lane; i < nblk && layout_ok; i += 32) {
+            const int sb = sb0 + i;
+            int j = -1, lb = sb, lo = 0, hi = ush;
+            if (sb >= nsb) {
+                j = 0;
+                while (j + 1 < un && useg[j + 1] <= sb) ++j;
+                lb = fb + (sb - useg[j]);
+                lo = ush;
+                hi = ulen[j];
+            }
+            int b = __ldg(a.block_tables + static_cast<int64_t>(s + max(j, 0)) * a.max_blocks_per_seq + lb);
+            if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
+                raise_error(a.err, kErrBounds);
+                b = -1;                             // outside the tensor map: TMA fills zeros, reads nothing
+            }
+            tbl[i] = b;
+            const int vlo = min(max(lo - (lb << lbs), 0), bs), vhi = min(max(hi - (lb << lbs), 0), bs);
+            udesc[i] = (j + 1) | (vlo << 8) | (vhi << 16);
+        }
+        __syncwarp();
+        if (a.k_new != nullptr && layout_ok) {
+            // Fused slot writes of the unit: member j's new token goes to position L_j - 1,
+            // which must lie in its own segment (a block holding it is private after
+            // copy-on-write) and be staged by this partition; a slot in the shared prefix is
+            // refused.  Done before the CTA barrier; one proxy fence orders them all before
+            // the tile loads.
+            bool stored = false;
+            for (int j = 0; j < un; ++j) {
+                const int64_t slot = __shfl_sync(0xffffffffu, uslot, j);
+                if (slot < 0) continue;
+                const int pos = __shfl_sync(0xffffffffu, Lj, j) - 1;
+                if (pos < ush) {
+                    if (lane == 0) raise_error(a.err, kErrBounds);
+                    continue;
+                }
+                const int i = useg[j] + ((pos >> lbs) - fb) - sb0;
+                if (i < 0 || i >= nblk) continue;   // another partition of the unit holds it
+                const int pb = tbl[i];
+                if (pb < 0 || slot != static_cast<int64_t>(pb) * bs + (pos & (bs - 1))) {
+                    if (lane == 0) raise_error(a.err, kErrBounds);
+                    continue;
+                }
+                if (lane < 2 * kHV) {
+                    uint4 r = urow[0];
+#pragma unroll
+                    for (int jj = 1; jj < kUnitRows; ++jj)
+                        if (j == jj) r = urow[jj];
+                    if (j >= kUnitRows) {
+                        const uint4* src = lane < kHV ? a.k_new : a.v_new;
+                        r = __ldg(src + (static_cast<int64_t>(s + j) * a.num_kv_heads + kvh) * kHV + lane % kHV);
+                    }
+                    const int64_t at = (slot * a.num_kv_heads + kvh) * kHV + lane % kHV;
+                    reinterpret_cast<uint4*>(lane < kHV ? a.key_cache : a.value_cache)[at] = r;
+                    stored = true;
+                }
+            }
+            if (stored) fence_proxy_async_global();
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -231,20 +370,22 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         fence_barrier_init();
     }
     __syncthreads();
+    if (grouped && ulen[kHeadsPerCta]) return;      // a unit whose layout the plan did not make
 
     // ================================================================ producer warp
     if (warp == CW) {
-        const int nblk = (end - start + bs - 1) / bs;
+        if (!grouped) {                             // (a unit's blocks were staged before the barrier)
 #pragma unroll
-        for (int k = 0; k < kTePerLane; ++k) {
-            const int i = lane + 32 * k;
-            if (32 * k < nblk && i < nblk) {
-                int b = te[k];
-                if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
-                    raise_error(a.err, kErrBounds);
-                    b = -1;                         // outside the tensor map: TMA fills zeros, reads nothing
+            for (int k = 0; k < kTePerLane; ++k) {
+                const int i = lane + 32 * k;
+                if (32 * k < nblk && i < nblk) {
+                    int b = te[k];
+                    if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
+                        raise_error(a.err, kErrBounds);
+                        b = -1;                     // outside the tensor map: TMA fills zeros, reads nothing
+                    }
+                    tbl[i] = b;
                 }
-                tbl[i] = b;
             }
         }
         __syncwarp();
@@ -308,6 +449,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     // causal limits of this lane's two query-row columns (all L for decode)
     const int lim0 = vh0 + 2 * (lane & 3) < a.group ? dec::causal_limit<MQ>(a, L, vh0 + 2 * (lane & 3)) : L;
     const int lim1 = vh0 + 2 * (lane & 3) + 1 < a.group ? dec::causal_limit<MQ>(a, L, vh0 + 2 * (lane & 3) + 1) : L;
+    // a unit: the members of this lane's two columns
+    const int mem0 = (2 * (lane & 3)) / a.group, mem1 = (2 * (lane & 3) + 1) / a.group;
     bool ok = !*abort_flag;
     unsigned epi_uses = 0;
     auto epi_sync = [&]() -> bool {               // all consumer threads, bounded
@@ -330,13 +473,39 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         const int tokw = start + c * kChunk + warp * 16;
         const int nv = min(16, end - tokw);
         if (nv > 0) {
-            if constexpr (KV8)
+            if constexpr (KV8) {
                 dec::consume_chunk_fp8<CW, MQ>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage),
                                                nv, warp, lane, sl2, tokw, lim0, lim1);
-            else
-                dec::consume_chunk<T, D, CW, MQ>(ws, smem_u32(kring + st * G::kStage),
-                                                 smem_u32(vring + st * G::kStage), nv, warp, lane, a.scale_log2, tokw,
-                                                 lim0, lim1);
+            } else {
+                const int r0 = lane >> 2;
+                unsigned vis, zr;
+                if (grouped) {
+                    // row r of this tile: valid within its block's segment; seen by the
+                    // columns of every member (shared prefix) or of its own member
+                    auto row_seg = [&](int r) -> int {  // segment (-1: prefix) or -2: no token
+                        if (r >= nv) return -2;
+                        const int sp = tokw + r;
+                        const int d = udesc[(sp >> lbs) - sb0];
+                        const int o = sp & (bs - 1);
+                        return (o >= ((d >> 8) & 0xFF) && o < (d >> 16)) ? (d & 0xFF) - 1 : -2;
+                    };
+                    const int ga = row_seg(r0), gb = row_seg(r0 + 8);
+                    vis = ((ga == -1 || ga == mem0) ? 1u : 0u) | ((ga == -1 || ga == mem1) ? 2u : 0u) |
+                          ((gb == -1 || gb == mem0) ? 4u : 0u) | ((gb == -1 || gb == mem1) ? 8u : 0u);
+                    zr = __ballot_sync(0xffffffffu, lane < 16 && row_seg(lane) == -2) & 0xFFFFu;
+                } else if constexpr (MQ) {
+                    const bool va = r0 < nv, vb = r0 + 8 < nv;
+                    const int pa = tokw + r0, pb = pa + 8;
+                    vis = ((va && pa < lim0) ? 1u : 0u) | ((va && pa < lim1) ? 2u : 0u) | ((vb && pb < lim0) ? 4u : 0u) |
+                          ((vb && pb < lim1) ? 8u : 0u);
+                    zr = dec::tail_rows(nv);
+                } else {
+                    vis = dec::tile_vis(r0 < nv, r0 + 8 < nv);
+                    zr = dec::tail_rows(nv);
+                }
+                dec::consume_chunk<T, D, CW>(ws, smem_u32(kring + st * G::kStage), smem_u32(vring + st * G::kStage),
+                                             zr, vis, MQ || grouped, warp, lane, a.scale_log2);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
@@ -363,7 +532,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     else
         dec::warp_state_to_smem<D, CW>(ws, scratch, warp, lane);
     if (!epi_sync()) return;
-    dec::combine_warps<T, D, CW, MQ>(a, scratch, sh0, s, kvh, vh0, gc, part, nparts, threadIdx.x);
+    dec::combine_warps<T, D, CW, MQ>(a, scratch, rows, gc, part, nparts, threadIdx.x, MQ || grouped);
     if (nparts == 1) return;
     // The group barrier orders every thread's partial writes before thread 0's
     // gpu-scope fence, which releases them all before the ticket.
@@ -379,20 +548,20 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
     if (!epi_sync()) return;
     if (!*merge_flag) return;
     // last partition of this (sequence, head group) to finish: merge them all
-    dec::merge_partitions<T, D, CW, MQ>(a, scratch, sh0, s, kvh, vh0, gc, nparts, warp, lane, threadIdx.x, epi_sync);
+    dec::merge_partitions<T, D, CW, MQ>(a, scratch, rows, gc, nparts, warp, lane, threadIdx.x, epi_sync);
 }
 
-template <typename T, int D, int CW, int STAGES, bool MQ = false, bool KV8 = false>
+template <typename T, int D, int CW, int STAGES, bool MQ = false, bool KV8 = false, bool UNITS = false>
 cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t s) {
-    constexpr size_t smem = Smem<D, CW, STAGES, KV8 ? 1 : 2>::kBytes;
+    constexpr size_t smem = Smem<D, CW, STAGES, KV8 ? 1 : 2, UNITS && !MQ && !KV8>::kBytes;
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = decode_kernel<T, D, CW, STAGES, MQ, KV8>;
+    auto kern = decode_kernel<T, D, CW, STAGES, MQ, KV8, UNITS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = a.plan ? dim3(nh * static_cast<unsigned>(a.plan_capacity))
-                         : dim3(nh, static_cast<unsigned>(a.max_parts), static_cast<unsigned>(a.num_seqs));
+                         : dim3(nh, static_cast<unsigned>(a.direct_parts), static_cast<unsigned>(a.num_seqs));
     cfg.blockDim = dim3(Geo<D, CW>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -423,6 +592,8 @@ cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& tmk, const CUtens
         return cudaErrorInvalidValue;
     }
     if (a.num_queries > 1) return launch_t<T, D, kCW, kStages16, true>(a, tmk, tmv, s);
+    // the plan may serve forks of one prompt as shared-prefix units: the kernel that reads them
+    if (a.units) return launch_t<T, D, kCW, kStages16, false, false, true>(a, tmk, tmv, s);
     return launch_t<T, D, kCW, kStages16>(a, tmk, tmv, s);
 }
 
@@ -435,7 +606,7 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_heads, int num_kv_
     const int parts = max_parts > 1 ? max_parts : 1;
     DecodeWorkspace w;
     w.ticket_bytes = pad(sizeof(unsigned) * static_cast<size_t>(num_seqs) * nh);
-    w.plan_bytes = pad(sizeof(int4) * static_cast<size_t>(num_seqs) * parts);
+    w.plan_bytes = pad(kPlanEntryInts * sizeof(int4) * static_cast<size_t>(num_seqs) * parts);
     const size_t sh = static_cast<size_t>(num_seqs) * num_heads * (max_parts > 1 ? max_parts : 0);
     w.o_bytes = pad(sh * head_dim * sizeof(float));
     w.ml_bytes = pad(sh * 2 * sizeof(float));

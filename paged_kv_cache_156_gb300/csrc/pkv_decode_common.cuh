@@ -13,7 +13,7 @@ namespace pkv {
 namespace dec {
 
 constexpr int kMaxTable = kPlanTableEntries;   // staged table entries: part_tokens (<= 4096) / block_size (>= 8)
-constexpr int kHeadsPerCta = 8;      // mma N: query heads served by one CTA
+constexpr int kHeadsPerCta = dec_heads_per_cta();   // mma N: query rows served by one CTA
 
 // CW consumer warps each own 16 positions of a chunk of 16 * CW positions;
 // EB is the pool's element size (2: fp16 / bf16; 1: E4M3 codes).
@@ -108,29 +108,39 @@ __device__ __forceinline__ void reset_state(WarpState<D>& w) {
     w.l0 = w.l1 = 0.0f;
 }
 
+// Score masks of one lane for one 16-position tile: bit 0 (row r0, column
+// 2t), bit 1 (row r0, column 2t + 1), bit 2 (row r0 + 8, column 2t), bit 3
+// (row r0 + 8, column 2t + 1), with r0 = lane / 4 and t = lane % 4.  A tile's
+// zero-row mask has bit r set for each of its 16 rows that holds no token
+// (past the stream, or a slot outside every column's range).
+__device__ __forceinline__ unsigned tile_vis(bool va, bool vb) { return (va ? 3u : 0u) | (vb ? 12u : 0u); }
+__device__ __forceinline__ unsigned tail_rows(int nv) { return nv < 16 ? (0xFFFFu << max(nv, 0)) & 0xFFFFu : 0u; }
+
 // One warp's 16 positions of a chunk: S^T = K Q^T on the tensor cores, online
-// softmax over those scores (log2 domain, positions >= nv masked), then
-// O^T += V^T P^T.  `warp` selects the 16 rows of the chunk; kst / vst are the
-// stage's K and V ring addresses; tokw is the position of the warp's first
-// row and lim0 / lim1 the causal limits of this lane's two head columns.
-template <typename T, int D, int CW, bool MQ>
-__device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uint32_t vst, int nv, int warp, int lane,
-                                              float sl2, int tokw, int lim0, int lim1) {
+// softmax over those scores (log2 domain, masked by `vis`), then O^T += V^T
+// P^T.  `warp` selects the 16 rows of the chunk; kst / vst are the stage's K
+// and V ring addresses; rows in `zrows` have their V zeroed first (their
+// slots may hold NaN).  `guard`: a column may have seen no position yet (its
+// maximum is still -inf), so its rescale is 1 and its weights 0.
+template <typename T, int D, int CW>
+__device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uint32_t vst, unsigned zrows,
+                                              unsigned vis, bool guard, int warp, int lane, float sl2) {
     using G = Geo<D, CW>;
     using M = Mma<T>;
     const int krow = warp * 16 + (lane & 15);                     // ldmatrix row supplied by this lane (K)
     const int kcol = lane >> 4;                                    // +8 elements
     const int vrow = warp * 16 + (lane & 7) + ((lane >> 4) << 3);  // (V, transposed load)
     const int vcol = (lane >> 3) & 1;
-    const int r0 = lane >> 2;                                      // accumulator row (position) of c0/c1
-    if (nv < 16) {
-        // rows past seq_len hold no token: zero their V so 0-weights stay 0
-        const int nz = (16 - nv) * (D / 8);
-        for (int i = lane; i < nz; i += 32) {
-            const int r = warp * 16 + nv + i / (D / 8);
-            const int cc = i % (D / 8);
-            const uint32_t addr = swz(vst + (cc >> 3) * G::kPlane, r, cc & 7);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+    if (zrows) {
+        // rows that hold no token: zero their V so 0-weights stay 0
+        unsigned zr = zrows;
+        while (zr) {
+            const int r = warp * 16 + __ffs(zr) - 1;
+            zr &= zr - 1;
+            for (int cc = lane; cc < D / 8; cc += 32) {
+                const uint32_t addr = swz(vst + (cc >> 3) * G::kPlane, r, cc & 7);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+            }
         }
         fence_proxy_async_smem();                 // before the async proxy refills this stage
         __syncwarp();
@@ -144,13 +154,10 @@ __device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uin
         M::run(sacc, af, w.qb[ks][0], w.qb[ks][1]);
     }
     // ---- online softmax (log2 domain); columns are heads 2*(lane%4) + {0,1}
-    const bool va = r0 < nv, vb = r0 + 8 < nv;
-    const int pa = tokw + r0, pb = pa + 8;
-    // decode: every column sees every row below nv; verify: also below the column's causal limit
-    const float s0 = (va && (!MQ || pa < lim0)) ? sacc[0] * sl2 : -INFINITY;
-    const float s1 = (va && (!MQ || pa < lim1)) ? sacc[1] * sl2 : -INFINITY;
-    const float s2 = (vb && (!MQ || pb < lim0)) ? sacc[2] * sl2 : -INFINITY;
-    const float s3 = (vb && (!MQ || pb < lim1)) ? sacc[3] * sl2 : -INFINITY;
+    const float s0 = (vis & 1u) ? sacc[0] * sl2 : -INFINITY;
+    const float s1 = (vis & 2u) ? sacc[1] * sl2 : -INFINITY;
+    const float s2 = (vis & 4u) ? sacc[2] * sl2 : -INFINITY;
+    const float s3 = (vis & 8u) ? sacc[3] * sl2 : -INFINITY;
     float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -158,13 +165,13 @@ __device__ __forceinline__ void consume_chunk(WarpState<D>& w, uint32_t kst, uin
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(w.m0, mx0), mn1 = fmaxf(w.m1, mx1);
-    // verify: a column with no visible position yet keeps max -inf: scale 1, weights 0
-    // (decode never has one: row 0 of the warp is always visible)
-    const float al0 = (MQ && mn0 == -INFINITY) ? 1.0f : fast_exp2(w.m0 - mn0);
-    const float al1 = (MQ && mn1 == -INFINITY) ? 1.0f : fast_exp2(w.m1 - mn1);
+    // a column with no visible position yet keeps max -inf: scale 1, weights 0
+    // (a one-sequence decode item never has one: row 0 of the warp is always visible)
+    const float al0 = (guard && mn0 == -INFINITY) ? 1.0f : fast_exp2(w.m0 - mn0);
+    const float al1 = (guard && mn1 == -INFINITY) ? 1.0f : fast_exp2(w.m1 - mn1);
     w.m0 = mn0;
     w.m1 = mn1;
-    const float b0 = (MQ && mn0 == -INFINITY) ? 0.0f : mn0, b1 = (MQ && mn1 == -INFINITY) ? 0.0f : mn1;
+    const float b0 = (guard && mn0 == -INFINITY) ? 0.0f : mn0, b1 = (guard && mn1 == -INFINITY) ? 0.0f : mn1;
     const uint32_t p01 = M::pack(fast_exp2(s0 - b0), fast_exp2(s1 - b1));
     const uint32_t p23 = M::pack(fast_exp2(s2 - b0), fast_exp2(s3 - b1));
     const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);   // the weights PV actually uses
@@ -359,12 +366,32 @@ __device__ __forceinline__ void warp_state_to_smem(const WarpState<D>& w, float*
     }
 }
 
+// Where column hx of an item goes: its row of the split-K partials and its
+// row of the output (element offset / D).
+struct ItemRows {
+    int64_t sh0;          // partial (and decode output) row of column 0 of a one-sequence item
+    int s, kvh, vh0;
+    int unit;             // members of a shared-prefix unit (> 1), else 1
+    __device__ __forceinline__ int64_t unit_row(const DecodeArgs& a, int hx) const {
+        return static_cast<int64_t>(s + hx / a.group) * a.num_heads + kvh * a.group + hx % a.group;
+    }
+    template <bool MQ>
+    __device__ __forceinline__ int64_t ws(const DecodeArgs& a, int hx) const {
+        return unit > 1 ? unit_row(a, hx) : sh0 + hx;
+    }
+    template <bool MQ>
+    __device__ __forceinline__ int64_t out(const DecodeArgs& a, int hx) const {
+        return unit > 1 ? unit_row(a, hx) : qo_row<MQ>(a, sh0, s, kvh, vh0, hx);
+    }
+};
+
 // Combine the warps' states of one item (scratch written and synchronised):
 // a sequence of one partition gets its output; otherwise the partition's
-// (max, sum, unnormalised output) go to the workspace.
+// (max, sum, unnormalised output) go to the workspace.  `guard`: a column may
+// have seen nothing in this item (its warps' maxima are all -inf).
 template <typename T, int D, int CW, bool MQ>
-__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* scratch, int64_t sh0, int s, int kvh,
-                                              int vh0, int gc, int part, int nparts, int tid) {
+__device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* scratch, const ItemRows& rows, int gc,
+                                              int part, int nparts, int tid, bool guard) {
     const float* sm_m = scratch;
     const float* sm_l = sm_m + CW * kHeadsPerCta;
     const float* sm_o = sm_l + CW * kHeadsPerCta;
@@ -379,15 +406,15 @@ __device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* 
 #pragma unroll
         for (int w = 0; w < CW; ++w) {
             const float mw = sm_m[w * kHeadsPerCta + hx];
-            // verify: a warp that saw nothing adds nothing (decode: mx is finite, the weight is 0 anyway)
-            const float wt = (MQ && mw == -INFINITY) ? 0.0f : fast_exp2(mw - mx);
+            // a warp that saw nothing adds nothing (without the guard mx is finite and the weight 0 anyway)
+            const float wt = (guard && mw == -INFINITY) ? 0.0f : fast_exp2(mw - mx);
             den += wt * sm_l[w * kHeadsPerCta + hx];
             num += wt * sm_o[(w * kHeadsPerCta + hx) * D + d];
         }
         if (nparts == 1) {
-            out[qo_row<MQ>(a, sh0, s, kvh, vh0, hx) * D + d] = T(MQ ? (den > 0.0f ? num / den : 0.0f) : num / den);
+            out[rows.out<MQ>(a, hx) * D + d] = T(guard ? (den > 0.0f ? num / den : 0.0f) : num / den);
         } else {
-            const int64_t sh = sh0 + hx;
+            const int64_t sh = rows.ws<MQ>(a, hx);
             a.ws_o[(sh * a.max_parts + part) * D + d] = num;
             if (d == 0) a.ws_ml[sh * a.max_parts + part] = make_float2(mx, den);
         }
@@ -399,12 +426,12 @@ __device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* 
 // the denominator, into msm[8] / dsm[8].  `sync` separates the phases.
 // Phase B: each output element sums its partials with all their loads in flight.
 template <typename T, int D, int CW, bool MQ, typename Sync>
-__device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scratch, int64_t sh0, int s, int kvh,
-                                                 int vh0, int gc, int nparts, int warp, int lane, int tid, Sync&& sync) {
+__device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scratch, const ItemRows& rows, int gc,
+                                                 int nparts, int warp, int lane, int tid, Sync&& sync) {
     float* msm = scratch;
     float* dsm = scratch + kHeadsPerCta;
     for (int hx = warp; hx < gc; hx += CW) {
-        const float2* ml = a.ws_ml + (sh0 + hx) * a.max_parts;
+        const float2* ml = a.ws_ml + rows.ws<MQ>(a, hx) * a.max_parts;
         float mx = -INFINITY;
         for (int p = lane; p < nparts; p += 32) mx = fmaxf(mx, __ldcg(ml + p).x);
 #pragma unroll
@@ -446,7 +473,7 @@ __device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scr
 #pragma unroll
                 for (int k = 0; k < kAcc; ++k) {
                     const int hx = hb + k * kRows;
-                    const int64_t row = (sh0 + (hx < gc ? hx : 0)) * a.max_parts + p + j;
+                    const int64_t row = rows.ws<MQ>(a, hx < gc ? hx : 0) * a.max_parts + p + j;
                     e[j][k] = __ldcg(reinterpret_cast<const float*>(a.ws_ml + row));
                     v[j][k] = __ldcg(a.ws_o + row * D + d);
                 }
@@ -462,7 +489,7 @@ __device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scr
             for (int k = 0; k < kAcc; ++k) {
                 const int hx = hb + k * kRows;
                 if (hx < gc) {
-                    const int64_t row = (sh0 + hx) * a.max_parts + p;
+                    const int64_t row = rows.ws<MQ>(a, hx) * a.max_parts + p;
                     num[k] += fast_exp2(__ldcg(a.ws_ml + row).x - mk[k]) * __ldcg(a.ws_o + row * D + d);
                 }
             }
@@ -471,7 +498,7 @@ __device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scr
         for (int k = 0; k < kAcc; ++k) {
             const int hx = hb + k * kRows;
             if (hx < gc)
-                out[qo_row<MQ>(a, sh0, s, kvh, vh0, hx) * D + d] =
+                out[rows.out<MQ>(a, hx) * D + d] =
                     T(MQ ? (dsm[hx] > 0.0f ? num[k] / dsm[hx] : 0.0f) : num[k] / dsm[hx]);
         }
     }

@@ -63,8 +63,10 @@ struct DecodeArgs {
     const void* q;                   // [B][nq][Hq][D]
     const int32_t* block_tables;     // [B][max_blocks_per_seq]
     const int32_t* seq_lens;         // [B]
-    int4* plan;                      // [plan_capacity] work list (sequence, partition, length, partition
-                                     // tokens), written per call by the plan kernel; nullptr: direct grid
+    int4* plan;                      // [plan_capacity][2] work list, written per call by the plan kernel
+                                     // (nullptr: direct grid): (first sequence, partition, stream length,
+                                     // partition tokens), then (unit members, shared prefix length, lengths of
+                                     // the unit's first two sequences)
     unsigned* tickets;               // [B][num_kv_heads * head_groups] finished partitions (zeroed per call)
     float* ws_o;                     // [B][Hq*nq][max_parts][D] unnormalised partial outputs
     float2* ws_ml;                   // [B][Hq*nq][max_parts] (running max in log2 units, sum)
@@ -84,9 +86,14 @@ struct DecodeArgs {
                                      // plan kernel may use
     int part_auto;                   // with a plan: 1 = the plan kernel picks the partition size (>= part_tokens)
     int slots;                       // SMs x resident decode CTAs per SM (for the plan kernel's choice)
-    int max_parts;                   // ceil(max_seq_len / part_tokens): the partials' stride
+    int max_parts;                   // partials per query row: ceil(max_seq_len / part_tokens), plus one when
+                                     // shared-prefix units are possible (the partials' stride)
+    int direct_parts;                // ceil(max_seq_len / part_tokens): the direct grid's partition extent
     int plan_capacity;               // entries of `plan` the grid covers (<= num_seqs * max_parts)
     int64_t sum_seq_lens;            // the caller's sum of seq_lens (0: not given); the plan checks it
+    int units;                       // 1: the plan may serve adjacent sequences that share leading blocks
+                                     // (forks of one prompt) as one unit (16-bit decode, <= 4 query heads
+                                     // per KV head: the members' heads fill one CTA's 8 columns)
     float scale_log2;                // scale * log2(e)
     int kv8;                         // 1: the pools hold E4M3 codes (head_dim 128), scaled per KV head
     const float* k_scale;            // [num_kv_heads] (E4M3 pools only)
@@ -106,6 +113,17 @@ struct DecodeArgs {
 // direct grid (one CTA per (KV head group, partition, sequence)).
 constexpr int kPlanMaxSeqs = 1024;
 
+// Shared-prefix units.  Adjacent sequences whose block tables agree on a
+// leading run of blocks (forks of one prompt, copy-on-write after the fork)
+// hold the same K/V there.  The plan serves up to 8 / (query heads per KV
+// head) of them as one unit: the unit's stream is the shared prefix once,
+// then each member's own blocks from the end of the prefix, block-aligned;
+// a member's query heads attend to the prefix and to its own segment only.
+// A unit shares at least this many positions (shorter runs stay separate).
+constexpr int kUnitMinShare = 256;
+// Work-list entries are two int4 each.
+constexpr int kPlanEntryInts = 2;
+
 // Block-table entries a decode CTA stages (a partition spans at most this many blocks).
 constexpr int kPlanTableEntries = 512;
 // Automatic partition sizes are multiples of this many positions.
@@ -123,6 +141,9 @@ __host__ __device__ inline long long plan_rule_tokens(long long sum_lens, long l
     const long long p = ((target + kPlanGranule / 2) / kPlanGranule) * kPlanGranule;
     return p > kPlanGranule ? p : kPlanGranule;
 }
+
+// Query rows (mma columns) one decode CTA serves.
+constexpr int dec_heads_per_cta() { return 8; }
 
 // Workspace layout of one decode call:
 //   [tickets | work list | partial outputs | (max, sum) pairs]

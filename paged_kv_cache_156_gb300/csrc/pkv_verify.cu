@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(Geo<D, kVW>::kThreads, 2) verify_kernel(const 
     if (a.plan) {
         const unsigned y = blockIdx.x / static_cast<unsigned>(nh);
         hh = static_cast<int>(blockIdx.x - y * static_cast<unsigned>(nh));
-        const int4 it = __ldg(a.plan + y);
+        const int4 it = __ldg(a.plan + kPlanEntryInts * y);   // (this kernel's plans have one-sequence units)
         s = it.x;
         part = it.y;
         L = it.z;
@@ -498,7 +498,7 @@ cudaError_t launch_verify_k(const DecodeArgs& a, const CUtensorMap& tmk, const C
     const unsigned nh = static_cast<unsigned>(a.num_kv_heads * a.head_groups);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = a.plan ? dim3(nh * static_cast<unsigned>(a.plan_capacity))
-                         : dim3(nh, static_cast<unsigned>(a.max_parts), static_cast<unsigned>(a.num_seqs));
+                         : dim3(nh, static_cast<unsigned>(a.direct_parts), static_cast<unsigned>(a.num_seqs));
     cfg.blockDim = dim3(Geo<D, kVW>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

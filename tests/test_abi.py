@@ -129,13 +129,17 @@ def test_workspace_formula(lib):
     B, Hq, Hkv, d = 16, 64, 8, 128
     pad = lambda x: (x + 255) // 256 * 256
     tickets = pad(4 * B * Hkv)                # one ticket per (sequence, KV head)
-    # one partition: no partials, one 16-byte work-list entry per sequence
-    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 512, 512) == tickets + pad(16 * B)
+    # one partition: no partials, one 32-byte work-list entry per sequence
+    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 512, 512) == tickets + pad(32 * B)
     n = lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 4096, 512)
     sh = B * Hq * 8
-    assert n == tickets + pad(16 * B * 8) + pad(sh * d * 4) + pad(sh * 8)
+    assert n == tickets + pad(32 * B * 8) + pad(sh * d * 4) + pad(sh * 8)
     # more than 8 query heads per KV head: one ticket per 8-head group
-    assert lib.pkv_decode_workspace_bytes(2, 64, 2, d, 64, 64) == pad(4 * 2 * 2 * 4) + pad(16 * 2)
+    assert lib.pkv_decode_workspace_bytes(2, 64, 2, d, 64, 64) == pad(4 * 2 * 2 * 4) + pad(32 * 2)
+    # at most 4 query heads per KV head (shared-prefix units possible): one spare partition per row
+    n = lib.pkv_decode_workspace_bytes(B, 32, Hkv, d, 4096, 512)
+    sh = B * 32 * 9
+    assert n == tickets + pad(32 * B * 9) + pad(sh * d * 4) + pad(sh * 8)
     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, 96, 4096, 512) == ctypes.c_size_t(-1).value
     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, 4096, 100) == ctypes.c_size_t(-1).value
 
