@@ -381,12 +381,11 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     // more than kVerifyMinRows query rows per KV head: the verify kernel, 32 or 64 rows per CTA
     // (E4M3 pools: the decode kernel's multi-query form, 8 rows per CTA, for any row count)
     const bool verify_kernel = num_queries > 1 && a.group > pkv::kVerifyMinRows && !kv8;
-    a.head_groups = verify_kernel ? (a.group + pkv::verify_rows_per_cta(a.group) - 1) / pkv::verify_rows_per_cta(a.group)
-                                  : (a.group + 7) / 8;
+    a.head_groups = verify_kernel ? (a.group + pkv::kVerifyTcRows - 1) / pkv::kVerifyTcRows : (a.group + 7) / 8;
     a.block_size = block_size;
     a.part_tokens = part;
     a.part_auto = partition_tokens == 0;
-    a.slots = sm_count_of(dev) * (verify_kernel ? pkv::verify_ctas_per_sm(head_dim, a.group)
+    a.slots = sm_count_of(dev) * (verify_kernel ? pkv::verify_tc_ctas_per_sm(head_dim)
                                                 : pkv::decode_ctas_per_sm(head_dim, kv8));
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
@@ -426,8 +425,8 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
         a.key_cache = const_cast<void*>(key_cache);
         a.value_cache = const_cast<void*>(value_cache);
     }
-    cudaError_t e = verify_kernel ? pkv::launch_verify(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
-                                                       static_cast<cudaStream_t>(stream), mode)
+    cudaError_t e = verify_kernel ? pkv::launch_verify_tc(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
+                                                          static_cast<cudaStream_t>(stream), mode)
                                   : pkv::launch_decode(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
                                                        static_cast<cudaStream_t>(stream), mode);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));

@@ -180,6 +180,15 @@ cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
                           int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
 int verify_ctas_per_sm(int head_dim, int rows);   // rows: query rows per KV head
 
+// The verify kernel on the fifth-generation tensor cores (tcgen05): up to
+// kVerifyTcRows query rows per CTA (head_groups = ceil(rows / kVerifyTcRows));
+// a KV head with at most 64 rows runs the M = 64 form.
+constexpr int kVerifyTcRows = 128;
+int verify_tc_rows_per_cta(int rows);
+cudaError_t launch_verify_tc(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
+                             int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
+int verify_tc_ctas_per_sm(int head_dim);
+
 // CTAs of the decode kernel resident per SM on the current device (current
 // configuration; kv8: the E4M3-pool kernel), or 0 if it cannot be queried.
 int decode_ctas_per_sm(int head_dim, bool kv8 = false);
