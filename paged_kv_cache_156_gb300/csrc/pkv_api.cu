@@ -387,6 +387,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.part_auto = partition_tokens == 0;
     a.slots = sm_count_of(dev) * (verify_kernel ? pkv::verify_tc_ctas_per_sm(head_dim)
                                                 : pkv::decode_ctas_per_sm(head_dim, kv8));
+    a.rule_weight = verify_kernel ? pkv::kRuleVerifyTc : kv8 ? pkv::kRuleDecode8 : pkv::kRuleDecode;
     a.max_seq_len = max_seq_len;
     a.max_parts = static_cast<int>(max_parts);
     a.direct_parts = static_cast<int>(base_parts);
@@ -401,7 +402,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
             // span) unless every sequence fits one partition; later adjustments only lower the
             // item count.  So at most B + sum / pb items, and B when no length exceeds pb.
             const int64_t nh = static_cast<int64_t>(a.num_kv_heads) * a.head_groups;
-            const int64_t rule = pkv::plan_rule_tokens(sum_seq_lens, nh, kv8, a.slots > 0 ? a.slots : 1);
+            const int64_t rule = pkv::plan_rule_tokens(sum_seq_lens, nh, a.rule_weight, a.slots > 0 ? a.slots : 1);
             const int64_t pb = std::min<int64_t>(std::max<int64_t>(rule, part),
                                                  static_cast<int64_t>(pkv::kPlanTableEntries) * block_size);
             const int64_t bound = static_cast<int64_t>(num_seqs) + (max_seq_len > pb ? sum_seq_lens / pb : 0);

@@ -10,9 +10,10 @@
 // partition) items that exist, in an order that starts long sequences first:
 //
 //  * partition size: at least the host's choice; when the call asks for the
-//    automatic size, about 0.85 x the positions per resident CTA slot
-//    (sum_s L_s * KV head groups / slots; 1.4 times that for an E4M3 pool,
-//    whose positions are half the bytes), in multiples of 512, capped by the
+//    automatic size, a kernel-specific fraction of the positions per resident
+//    CTA slot (sum_s L_s * KV head groups / slots: 0.85 of it for the 16-bit
+//    decode kernel, 1.2 for an E4M3 pool, whose positions are half the bytes,
+//    1.1 for the tensor-core verify kernel), in multiples of 512, capped by the
 //    longest sequence and by the staged table, raised when the item count
 //    would spill a quarter wave or less past one full wave, then shrunk to
 //    the smallest multiple of 64 that splits the longest sequence into as
@@ -297,8 +298,8 @@ __global__ void __launch_bounds__(kPlanMaxSeqs) plan_kernel(const DecodeArgs a) 
     int P0 = a.part_tokens, q0 = a.part_tokens;
     int cap = a.part_tokens;
     if (a.part_auto) {
-        // 0.85 x the positions per slot (an E4M3 position counts 1.4 times), from the lengths' sum
-        const long long p = plan_rule_tokens(W, nh, a.kv8 != 0, slots);
+        // the kernel's share of the positions per slot (plan_rule_tokens), from the lengths' sum
+        const long long p = plan_rule_tokens(W, nh, a.rule_weight, slots);
         const int table_cap = dec::kMaxTable * bs;
         cap = max(a.part_tokens, min(table_cap, (lmax_u + 63) / 64 * 64));
         P0 = static_cast<int>(min(max(p, static_cast<long long>(a.part_tokens)), static_cast<long long>(cap)));

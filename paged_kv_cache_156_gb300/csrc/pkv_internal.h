@@ -86,6 +86,7 @@ struct DecodeArgs {
                                      // plan kernel may use
     int part_auto;                   // with a plan: 1 = the plan kernel picks the partition size (>= part_tokens)
     int slots;                       // SMs x resident decode CTAs per SM (for the plan kernel's choice)
+    int rule_weight;                 // the automatic partition rule's weight (twentieths; plan_rule_tokens)
     int max_parts;                   // partials per query row: ceil(max_seq_len / part_tokens), plus one when
                                      // shared-prefix units are possible (the partials' stride)
     int direct_parts;                // ceil(max_seq_len / part_tokens): the direct grid's partition extent
@@ -130,14 +131,20 @@ constexpr int kPlanTableEntries = 512;
 constexpr int kPlanGranule = 512;
 
 // The plan kernel's automatic partition size from the lengths' sum alone:
-// about 0.85 x the positions per resident CTA slot (sum * nh / slots); an E4M3
-// position counts as 1.4 of them (half the bytes of a 16-bit one, the same
-// arithmetic and per-CTA costs; measured best on the 8B-shaped batch: 3072
-// positions against 4096 at twice), rounded to the nearest multiple of
-// kPlanGranule, at least one granule.  The host uses the same rule to bound
-// the work list the grid must cover.
-__host__ __device__ inline long long plan_rule_tokens(long long sum_lens, long long nh, bool kv8, long long slots) {
-    const long long target = (sum_lens * nh * (kv8 ? 24 : 17)) / (slots * 20);
+// about w / 20 of the positions per resident CTA slot (sum * nh / slots),
+// rounded to the nearest multiple of kPlanGranule, at least one granule.  The
+// weight w (twentieths) is the kernel's: kRuleDecode for the 16-bit decode
+// kernel (0.85), kRuleDecode8 for E4M3 pools (an E4M3 position is half the
+// bytes of a 16-bit one, with the same arithmetic and per-CTA costs; measured
+// best on the 8B-shaped batch: 3072 positions against 4096 at twice), and
+// kRuleVerifyTc for the tensor-core verify kernel, whose items carry a longer
+// start-up and epilogue.  The host uses the same rule to bound the work list
+// the grid must cover.
+constexpr int kRuleDecode = 17;
+constexpr int kRuleDecode8 = 24;
+constexpr int kRuleVerifyTc = 22;
+__host__ __device__ inline long long plan_rule_tokens(long long sum_lens, long long nh, int weight, long long slots) {
+    const long long target = (sum_lens * nh * weight) / (slots * 20);
     const long long p = ((target + kPlanGranule / 2) / kPlanGranule) * kPlanGranule;
     return p > kPlanGranule ? p : kPlanGranule;
 }

@@ -43,6 +43,7 @@
 // CTA that takes the last ticket merges them (split-K), as decode does.
 // Every wait is bounded in wall time; a CTA that gives up raises the error
 // word, waits (bounded) for its own MMAs and frees its TMEM.
+#include <algorithm>
 #include <atomic>
 
 #include "pkv_decode_common.cuh"
@@ -688,8 +689,16 @@ __global__ void __launch_bounds__(TcGeo<D, M>::kThreads, 2) verify_tc_kernel(con
         if (tk == static_cast<unsigned>(nparts - 1)) *ticket = 0u;   // reset for the next run
     }
     if (!epi_sync()) return;
-    if (!*merge_flag || !has_row) return;
-    const float2* ml = a.ws_ml + (prow0 + row) * a.max_parts;
+    if (!*merge_flag) return;
+    // every softmax thread merges: 128 / M threads a row, D * M / 128 columns each, 16 columns
+    // and four partitions' loads in flight at a time (partitions summed in order)
+    constexpr int kTpr = TG::kSoftmaxThreads / M;   // threads per row
+    constexpr int kCols = D / kTpr;                 // columns per thread
+    const int mrow = rg * TG::kRows + static_cast<int>(threadIdx.x) / kTpr;
+    if (mrow >= R) return;
+    const int cb = (static_cast<int>(threadIdx.x) % kTpr) * kCols;
+    const float2* ml = a.ws_ml + (prow0 + mrow) * a.max_parts;
+    const float* wo = a.ws_o + (prow0 + mrow) * a.max_parts * D;
     float mmax = -INFINITY;
     for (int p = 0; p < nparts; ++p) mmax = fmaxf(mmax, __ldcg(ml + p).x);
     float den = 0.0f;
@@ -698,30 +707,48 @@ __global__ void __launch_bounds__(TcGeo<D, M>::kThreads, 2) verify_tc_kernel(con
         den += e.x == -INFINITY ? 0.0f : fast_exp2(e.x - mmax) * e.y;
     }
     const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-    T* orow = out + tc_row_offset(a, s, kvh, row) * D;
-    for (int c0 = 0; c0 < D; c0 += 32) {
-        float num[32];
+    T* orow = out + tc_row_offset(a, s, kvh, mrow) * D;
+#pragma unroll 1
+    for (int c0 = cb; c0 < cb + kCols; c0 += 16) {
+        float num[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) num[j] = 0.0f;
-        for (int p = 0; p < nparts; ++p) {
-            const float2 e = __ldcg(ml + p);
-            const float w = e.x == -INFINITY ? 0.0f : fast_exp2(e.x - mmax);
-            const float4* src = reinterpret_cast<const float4*>(a.ws_o + ((prow0 + row) * a.max_parts + p) * D + c0);
+        for (int j = 0; j < 16; ++j) num[j] = 0.0f;
+#pragma unroll 1
+        for (int p0 = 0; p0 < nparts; p0 += 4) {
+            float w[4];
+            float4 v[4][4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 v = __ldcg(src + j);
-                num[4 * j] += w * v.x;
-                num[4 * j + 1] += w * v.y;
-                num[4 * j + 2] += w * v.z;
-                num[4 * j + 3] += w * v.w;
+            for (int q = 0; q < 4; ++q) {
+                const int p = p0 + q;
+                w[q] = 0.0f;
+                if (p < nparts) {
+                    const float2 e = __ldcg(ml + p);
+                    w[q] = e.x == -INFINITY ? 0.0f : fast_exp2(e.x - mmax);
+                    const float4* src = reinterpret_cast<const float4*>(wo + static_cast<int64_t>(p) * D + c0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[q][j] = __ldcg(src + j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[q][j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    num[4 * j] += w[q] * v[q][j].x;
+                    num[4 * j + 1] += w[q] * v[q][j].y;
+                    num[4 * j + 2] += w[q] * v[q][j].z;
+                    num[4 * j + 3] += w[q] * v[q][j].w;
+                }
             }
         }
-        uint32_t wv[16];
+        uint32_t wv[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) wv[j] = pack2<T>(num[2 * j] * inv, num[2 * j + 1] * inv);
+        for (int j = 0; j < 8; ++j) wv[j] = pack2<T>(num[2 * j] * inv, num[2 * j + 1] * inv);
         uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     }
 }
 
@@ -778,21 +805,36 @@ cudaError_t launch_verify_tc(const DecodeArgs& a, const CUtensorMap& tmk, const 
 
 int verify_tc_rows_per_cta(int rows) { return rows <= 64 ? 64 : kVerifyTcRows; }
 
+// CTAs of the verify kernel an SM holds at once, from its resources: tensor memory (each CTA
+// allocates kTmemCols of the SM's 512 columns), shared memory, and registers, where an SM's
+// four sub-partitions each hold a quarter of the register file and take the resident warps in
+// turn.  (cudaOccupancyMaxActiveBlocksPerMultiprocessor answers 1 for this kernel, while the
+// hardware runs 2 at a time on every SM; the partition rule needs the real count.)
 int verify_tc_ctas_per_sm(int head_dim) {
     static std::atomic<int> cache[2] = {-1, -1};   // head_dim 64, 128; the same on every GB300
     const int i = head_dim == 64 ? 0 : 1;
     int n = cache[i].load(std::memory_order_relaxed);
     if (n < 0) {
-        int k = 0;
-        auto query = [&](auto kern, size_t smem) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
-                    cudaSuccess &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, TcGeo<128, 128>::kThreads, smem) == cudaSuccess)
-                return k;
-            return 0;
+        auto fit = [](auto kern, size_t smem, int tmem_cols) -> int {
+            cudaFuncAttributes fa{};
+            int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
+                return 1;
+            const int warps = (TcGeo<128, 64>::kThreads + 31) / 32;
+            const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+            int k = 512 / tmem_cols;
+            while (k > 1 && (static_cast<size_t>(k) * (smem + reserved) > static_cast<size_t>(smem_sm) ||
+                             (k * warps + 3) / 4 * regs_warp > regs_sm / 4))
+                --k;
+            return k;
         };
-        n = i == 0 ? query(verify_tc_kernel<__half, 64, 128>, TcGeo<64, 128>::kBytes)
-                   : query(verify_tc_kernel<__half, 128, 128>, TcGeo<128, 128>::kBytes);
+        n = i == 0 ? std::min(fit(verify_tc_kernel<__half, 64, 128>, TcGeo<64, 128>::kBytes, TcGeo<64, 128>::kTmemCols),
+                              fit(verify_tc_kernel<__half, 64, 64>, TcGeo<64, 64>::kBytes, TcGeo<64, 64>::kTmemCols))
+                   : std::min(fit(verify_tc_kernel<__half, 128, 128>, TcGeo<128, 128>::kBytes, TcGeo<128, 128>::kTmemCols),
+                              fit(verify_tc_kernel<__half, 128, 64>, TcGeo<128, 64>::kBytes, TcGeo<128, 64>::kTmemCols));
         cache[i].store(n, std::memory_order_relaxed);
     }
     return n;
