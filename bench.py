@@ -386,7 +386,11 @@ def run_pkv(args, rank, world, local):
             if fused:
                 if spec.fp8:
                     kw.update(k_scale=k_scales[l], v_scale=v_scales[l])
-                pkv.paged_kv_append_decode(outs[l], q, k_new, v_new, kcs[l], vcs[l], slots, tables, lens, **kw)
+                # layers after the first: nothing pending writes their pools, the tables or the
+                # plan (the preceding launch is the previous layer's), so their tile loads may
+                # start while it finishes
+                pkv.paged_kv_append_decode(outs[l], q, k_new, v_new, kcs[l], vcs[l], slots, tables, lens,
+                                           inputs_ready=l > 0, **kw)
             elif spec.fp8:
                 pkv.paged_attention_decode_fp8(outs[l], q, kcs[l], vcs[l], tables, lens, k_scales[l], v_scales[l], **kw)
             else:

@@ -258,6 +258,22 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void*
  *   kv_dt         dt for 16-bit pools, PKV_E4M3 for 8-bit pools (then
  *                 k_scale / v_scale as in pkv_paged_kv_append_fp8; else
  *                 ignored)
+ *   planned       0: plan and run; PKV_PLANNED: run over the plan
+ *                 pkv_decode_plan wrote; PKV_PLANNED | PKV_INPUTS_READY: that,
+ *                 and the caller guarantees that no work still pending on
+ *                 `stream` when this call is made writes the pools, the block
+ *                 tables, seq_lens or the workspace's plan (within a decode
+ *                 step: every layer after the first, whose pool only its own
+ *                 call writes).  Each CTA then reads its work item, stages its
+ *                 block-table slice and starts its first tile loads while the
+ *                 preceding kernel finishes (programmatic dependent launch),
+ *                 and waits for that kernel before it reads q, k, v or
+ *                 slot_mapping; the chunk that receives the new token is never
+ *                 loaded before its slot is written.  Results are the same bit
+ *                 for bit.  Not for the call right after pkv_decode_plan (it
+ *                 writes the plan) nor after pkv_copy_blocks / swap / append
+ *                 into the same pools.  16-bit pools only (ignored for E4M3).
+ *                 Any other value is PKV_ERR_INVALID.
  *   other arguments as pkv_paged_attention_decode / _planned.
  * A non-negative slot that is not that position's slot (or a sequence of
  * length 0 with one) is not written and raises the error word's bounds bit.
@@ -265,6 +281,8 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8_planned(void* out, const void*
  * sequence of the call (the block manager's copy-on-write gives every
  * sequence its own last block before it appends).
  */
+#define PKV_PLANNED 1
+#define PKV_INPUTS_READY 2
 PKV_API pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const void* k, const void* v,
                                       void* key_cache, void* value_cache, const int64_t* slot_mapping,
                                       const int32_t* block_tables, int max_blocks_per_seq,

@@ -26,6 +26,8 @@ PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, P
 _DT = {torch.float16: 0, torch.bfloat16: 1}
 _POOL_DT = {torch.float16: 0, torch.bfloat16: 1, torch.uint8: 2}   # uint8 pools hold E4M3 codes
 PLAN_MAX_SEQS = 1024        # PKV_PLAN_MAX_SEQS: batches up to this size run through the plan kernel
+PLANNED = 1                 # PKV_PLANNED: run over the plan an earlier call wrote
+INPUTS_READY = 2            # PKV_INPUTS_READY: nothing pending writes the pools, tables, lengths or plan
 
 # every symbol include/pkv.h declares
 ABI_SYMBOLS = ("pkv_version", "pkv_last_error", "pkv_paged_kv_append", "pkv_decode_workspace_bytes",
@@ -341,10 +343,15 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, seq
 @_one_device
 def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, block_tables, seq_lens, scale=None,
                            max_seq_len=None, workspace=None, partition_tokens=0, planned=False, sum_seq_lens=0,
-                           k_scale=None, v_scale=None) -> None:
+                           k_scale=None, v_scale=None, inputs_ready=False) -> None:
     """paged_kv_append of one new token per sequence (k, v [B, Hkv, d]; slot_mapping int64 [B], the slot of
     position seq_lens[s] - 1, or < 0 for none) then paged_attention_decode, in one launch.  uint8 pools hold
-    E4M3 codes and take k_scale / v_scale as paged_kv_append_fp8 does."""
+    E4M3 codes and take k_scale / v_scale as paged_kv_append_fp8 does.  ``inputs_ready`` (with ``planned``):
+    the caller guarantees that no work still pending on the stream writes the pools, block tables, seq_lens or
+    the workspace's plan (every layer of a step after the first), so the tile loads may start while the
+    preceding kernel finishes (``PKV_INPUTS_READY``)."""
+    if inputs_ready and not planned:
+        raise ValueError("inputs_ready needs planned=True (a plan written by an earlier call)")
     kv8 = key_cache.dtype == torch.uint8
     NB, bs, Hkv, d = _pool("key_cache", key_cache, tuple(_POOL_DT))
     if value_cache.shape != key_cache.shape or value_cache.dtype != key_cache.dtype:
@@ -376,7 +383,7 @@ def paged_kv_append_decode(out, q, k, v, key_cache, value_cache, slot_mapping, b
     _check(load().pkv_paged_kv_append_decode(
         *ptrs, block_tables.shape[1], ctypes.c_void_p(seq_lens.data_ptr()), B, int(max_seq_len), int(sum_seq_lens),
         Hq, Hkv, d, bs, NB, float(scale), _DT[q.dtype], _POOL_DT[key_cache.dtype], *scales, ws_ptr, ws_bytes,
-        int(partition_tokens), int(bool(planned)), _stream(q)))
+        int(partition_tokens), (PLANNED if planned else 0) | (INPUTS_READY if inputs_ready else 0), _stream(q)))
 
 
 @_one_device

@@ -283,6 +283,7 @@ struct NewTokens {
     const void* k;
     const void* v;
     const int64_t* slot_mapping;
+    bool inputs_ready;              // PKV_INPUTS_READY: pools, tables, lengths and plan final before the launch
 };
 
 // Decode (num_queries == 1) and multi-query verify share one path: a KV head
@@ -425,6 +426,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
         a.slot_mapping = fused->slot_mapping;
         a.key_cache = const_cast<void*>(key_cache);
         a.value_cache = const_cast<void*>(value_cache);
+        a.early = fused->inputs_ready && mode == pkv::DecodeMode::kRunOnly && a.plan != nullptr && !kv8 ? 1 : 0;
     }
     cudaError_t e = verify_kernel ? pkv::launch_verify_tc(a, tmk, tmv, dt == PKV_F16 ? 0 : 1, head_dim,
                                                           static_cast<cudaStream_t>(stream), mode)
@@ -546,6 +548,8 @@ pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const void* k, c
                                       size_t workspace_bytes, int partition_tokens, int planned, void* stream) {
     CallRange range_("pkv_paged_kv_append_decode");
     if (sum_seq_lens < 0) return fail(PKV_ERR_INVALID, "sum_seq_lens < 0");
+    if ((planned & ~(PKV_PLANNED | PKV_INPUTS_READY)) != 0 || planned == PKV_INPUTS_READY)
+        return fail(PKV_ERR_INVALID, "planned %d: 0, PKV_PLANNED or PKV_PLANNED | PKV_INPUTS_READY", planned);
     if (kv_dt == PKV_E4M3) {
         if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "E4M3 pools need k_scale and v_scale");
     } else if (kv_dt != dt) {
@@ -553,12 +557,12 @@ pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const void* k, c
     } else {
         k_scale = v_scale = nullptr;
     }
-    const NewTokens nt{k, v, slot_mapping};
+    const NewTokens nt{k, v, slot_mapping, (planned & PKV_INPUTS_READY) != 0};
     return attention_call(out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                           max_seq_len, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dt, 1,
                           workspace, workspace_bytes, partition_tokens, stream, k_scale, v_scale,
-                          planned ? pkv::DecodeMode::kRunOnly : pkv::DecodeMode::kPlanAndRun, false, sum_seq_lens,
-                          &nt);
+                          (planned & PKV_PLANNED) ? pkv::DecodeMode::kRunOnly : pkv::DecodeMode::kPlanAndRun, false,
+                          sum_seq_lens, &nt);
 }
 
 pkv_status pkv_paged_kv_append_fp8(const void* k, const void* v, void* key_cache, void* value_cache,

@@ -84,8 +84,11 @@ __device__ __forceinline__ uint32_t q_as_f16x2<__nv_bfloat16>(uint32_t x) {
 // KV8: the pools hold E4M3 codes (head_dim 128); the tensor cores run in f16.
 // UNITS: the work list may hold shared-prefix units (16-bit decode only; the
 // host launches this form when the plan may make them).
+// Register caps: an SM's four sub-partitions each hold a quarter of the register
+// file (16384) and take the resident warps in turn, so the 5-warp CTAs fit 3 to an
+// SM (head_dim 128, 16-bit) at 128 registers, 4 (E4M3) at 96, 6 (head_dim 64) at 64.
 template <typename T, int D, int CW, int STAGES, bool MQ, bool KV8 = false, bool UNITS = false>
-__global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __maxnreg__(KV8 ? 96 : D == 64 ? 64 : 128) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                      const __grid_constant__ CUtensorMap tmv,
                                                                      const DecodeArgs a) {
     static_assert(!KV8 || D == 128, "E4M3 pools: head_dim 128");
@@ -112,7 +115,10 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    grid_dependency_wait();                         // the plan and the pools come from earlier kernels
+    // the plan and the pools come from earlier kernels; with the caller's guarantee that
+    // nothing still running writes them (a.early), the wait moves below the work item,
+    // the table slice and the first tile loads, before anything else is read
+    if (!a.early) grid_dependency_wait();
     // Work item: from the plan (one entry per (unit, partition), KV head
     // groups innermost in the 1-D grid) or, without one, the 3-D grid itself.
     // A unit is one sequence, or (16-bit decode) `un` adjacent sequences that
@@ -155,6 +161,8 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         Lp = -1;
     }
     const bool grouped = kUnits && un > 1;          // a shared-prefix unit (CTA-uniform)
+    const bool early = a.early && a.plan && !grouped && !MQ && !KV8;   // (CTA-uniform)
+    if (a.early && !early) grid_dependency_wait();
     const int hg = hh % a.head_groups;
     const int kvh = hh / a.head_groups;
     const int vh0 = hg * kHeadsPerCta;                // first query row of this CTA within the KV head's rows
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
                 const int i = lane + 32 * k;
                 te[k] = (32 * k < tcount && i < tcount) ? __ldg(row + i) : 0;
             }
-            if (maybe_put) {
+            if (maybe_put && !early) {              // (early: after the wait, below)
                 nslot = __ldg(a.slot_mapping + s);
                 if (lane < 2 * kHV) {
                     const uint4* src = lane < kHV ? a.k_new : a.v_new;
@@ -211,6 +219,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
             ws.qb[ks][1] = n < gc ? q_as_f16x2<T>(raw.y) : 0u;
         }
     } else {
+        if (early) grid_dependency_wait();          // q comes from the preceding kernel
         // Q^T as the B operand (k = head_dim, n = query head): lane holds
         // q[n = lane/4][k = 16*ks + 2*(lane%4) + {0,1}] and the same at k + 8.
         const int n = lane >> 2;
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         }
     }
 
-    if (threadIdx.x == 0) {
+    auto init_barriers = [&]() {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], CW);
@@ -368,23 +377,75 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         *abort_flag = misaligned;
         *merge_flag = 0;
         fence_barrier_init();
+    };
+    // K/V bytes are read once per step: evict them first, so the small data every
+    // CTA and layer reuses (tables, q, work items, partials) stays in L2
+    auto issue_chunk = [&](int c, uint64_t pol) {
+        const int st = c % STAGES;
+        const int tok0 = start + c * kChunk;
+        const int nb = (min(end, tok0 + kChunk) - tok0 + bs - 1) / bs;
+        mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * kEB * 2));
+        for (int j = 0; j < nb; ++j) {
+            const int pb = tbl[c * (kChunk / bs) + j];
+#pragma unroll
+            for (int hf = 0; hf < G::kHalves; ++hf) {
+                const int off = st * G::kStage + hf * G::kPlane + j * bs * 128;
+                tma_load_4d_hint(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st], pol);
+                tma_load_4d_hint(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st], pol);
+            }
+        }
+    };
+    auto stage_table = [&]() {                      // the producer warp's table slice into shared memory
+#pragma unroll
+        for (int k = 0; k < kTePerLane; ++k) {
+            const int i = lane + 32 * k;
+            if (32 * k < nblk && i < nblk) {
+                int b = te[k];
+                if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
+                    raise_error(a.err, kErrBounds);
+                    b = -1;                         // outside the tensor map: TMA fills zeros, reads nothing
+                }
+                tbl[i] = b;
+            }
+        }
+        __syncwarp();
+    };
+    // chunks whose tile loads the producer issued before the wait (early only): the ring's
+    // first stages, up to the chunk that receives the new token (written after the wait)
+    int c_first = 0;
+    if (early && warp == CW) {
+        stage_table();
+        if (lane == 0) {
+            init_barriers();
+            if (!*abort_flag) {
+                prefetch_tensormap(&tmk);
+                prefetch_tensormap(&tmv);
+                const uint64_t pol = l2_policy_evict_first();
+                for (; c_first < min(STAGES, nchunks); ++c_first) {
+                    const int tok0 = start + c_first * kChunk;
+                    if (maybe_put && L - 1 >= tok0 && L - 1 < tok0 + kChunk) break;
+                    issue_chunk(c_first, pol);
+                }
+            }
+        }
+        c_first = __shfl_sync(0xffffffffu, c_first, 0);
+    } else if (!early && threadIdx.x == 0) {
+        init_barriers();
     }
     __syncthreads();
     if (grouped && ulen[kHeadsPerCta]) return;      // a unit whose layout the plan did not make
 
     // ================================================================ producer warp
     if (warp == CW) {
-        if (!grouped) {                             // (a unit's blocks were staged before the barrier)
-#pragma unroll
-            for (int k = 0; k < kTePerLane; ++k) {
-                const int i = lane + 32 * k;
-                if (32 * k < nblk && i < nblk) {
-                    int b = te[k];
-                    if (b < 0 || static_cast<int64_t>(b) >= a.num_blocks) {
-                        raise_error(a.err, kErrBounds);
-                        b = -1;                     // outside the tensor map: TMA fills zeros, reads nothing
-                    }
-                    tbl[i] = b;
+        // (a unit's blocks were staged before the barrier; early: with the first tile loads)
+        if (!grouped && !early) stage_table();
+        if (early) {
+            grid_dependency_wait();                 // the new token comes from the preceding kernel
+            if (maybe_put) {
+                nslot = __ldg(a.slot_mapping + s);
+                if (lane < 2 * kHV) {
+                    const uint4* src = lane < kHV ? a.k_new : a.v_new;
+                    nrow = __ldg(src + (static_cast<int64_t>(s) * a.num_kv_heads + kvh) * kHV + lane % kHV);
                 }
             }
         }
@@ -413,29 +474,15 @@ __global__ void __launch_bounds__(Geo<D, CW>::kThreads) decode_kernel(const __gr
         if (lane == 0 && !*abort_flag) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-            // K/V bytes are read once per step: evict them first, so the small data
-            // every CTA and layer reuses (tables, q, work items, partials) stays in L2
             const uint64_t pol = l2_policy_evict_first();
-            const int per_chunk = kChunk / bs;
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = c_first; c < nchunks; ++c) {
                 const int st = c % STAGES;
                 const unsigned ph = (c / STAGES) & 1;
                 if (!dec::wait_or_abort(&empty[st], ph ^ 1, abort_flag)) {
                     dec::raise_abort(a.err, abort_flag);
                     break;
                 }
-                const int tok0 = start + c * kChunk;
-                const int nb = (min(end, tok0 + kChunk) - tok0 + bs - 1) / bs;
-                mbar_arrive_expect_tx(&full[st], static_cast<unsigned>(nb * bs * D * kEB * 2));
-                for (int j = 0; j < nb; ++j) {
-                    const int pb = tbl[c * per_chunk + j];
-#pragma unroll
-                    for (int hf = 0; hf < G::kHalves; ++hf) {
-                        const int off = st * G::kStage + hf * G::kPlane + j * bs * 128;
-                        tma_load_4d_hint(kring + off, &tmk, hf * 64, kvh, 0, pb, &full[st], pol);
-                        tma_load_4d_hint(vring + off, &tmv, hf * 64, kvh, 0, pb, &full[st], pol);
-                    }
-                }
+                issue_chunk(c, pol);
             }
         }
         return;

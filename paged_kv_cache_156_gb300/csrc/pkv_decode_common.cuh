@@ -422,12 +422,59 @@ __device__ __forceinline__ void combine_warps(const DecodeArgs& a, const float* 
 }
 
 // Merge every partition of (sequence, head group) into the output; run by the
-// CTA that took the last ticket.  Phase A (one warp per head): the maximum and
-// the denominator, into msm[8] / dsm[8].  `sync` separates the phases.
-// Phase B: each output element sums its partials with all their loads in flight.
+// CTA that took the last ticket.  Up to four partitions: each thread first loads
+// every partition's value of its output elements (they do not depend on the
+// maxima), then one warp per head turns the partitions' (maximum, sum) pairs
+// into normalised weights in shared memory; one round trip in all.  More
+// partitions: phase A (one warp per head) puts the maximum and the denominator
+// into msm[8] / dsm[8]; `sync` separates the phases; phase B: each output
+// element sums its partials with four partitions' loads in flight.  Partitions
+// are summed in partition order either way.
 template <typename T, int D, int CW, bool MQ, typename Sync>
 __device__ __forceinline__ bool merge_partitions(const DecodeArgs& a, float* scratch, const ItemRows& rows, int gc,
                                                  int nparts, int warp, int lane, int tid, Sync&& sync) {
+    if (nparts <= 4) {
+        constexpr int kConsumers = 32 * CW;
+        static_assert(kConsumers >= D, "one pass over d");
+        constexpr int kRows = kConsumers / D;       // heads covered per pass
+        constexpr int kAcc = (kHeadsPerCta + kRows - 1) / kRows;
+        const int d = tid % D;
+        const int hb = tid / D;
+        float v[kAcc][4];
+#pragma unroll
+        for (int k = 0; k < kAcc; ++k) {
+            const int hx = hb + k * kRows;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[k][j] = (j < nparts && hx < gc) ? __ldcg(a.ws_o + (rows.ws<MQ>(a, hx) * a.max_parts + j) * D + d)
+                                                  : 0.0f;
+        }
+        float* wsm = scratch;                       // [kHeadsPerCta][4] normalised weights
+        for (int hx = warp; hx < gc; hx += CW) {
+            const float2 e = lane < nparts ? __ldcg(a.ws_ml + rows.ws<MQ>(a, hx) * a.max_parts + lane)
+                                           : make_float2(-INFINITY, 0.0f);
+            float mx = e.x;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float w = e.x == -INFINITY ? 0.0f : fast_exp2(e.x - mx);
+            float den = w * e.y;
+            den += __shfl_xor_sync(0xffffffffu, den, 1);
+            den += __shfl_xor_sync(0xffffffffu, den, 2);
+            if (lane < 4) wsm[hx * 4 + lane] = den > 0.0f ? w / den : 0.0f;
+        }
+        if (!sync()) return false;
+        T* out = reinterpret_cast<T*>(a.out);
+#pragma unroll
+        for (int k = 0; k < kAcc; ++k) {
+            const int hx = hb + k * kRows;
+            if (hx >= gc) continue;
+            float num = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) num += wsm[hx * 4 + j] * v[k][j];
+            out[rows.out<MQ>(a, hx) * D + d] = T(num);
+        }
+        return true;
+    }
     float* msm = scratch;
     float* dsm = scratch + kHeadsPerCta;
     for (int hx = warp; hx < gc; hx += CW) {

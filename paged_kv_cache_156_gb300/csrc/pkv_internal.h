@@ -108,6 +108,12 @@ struct DecodeArgs {
     const int64_t* slot_mapping = nullptr;   // [B]
     void* key_cache = nullptr;       // the pools written by the fused slot write
     void* value_cache = nullptr;
+    // 1: nothing still running before this launch writes the pools, block tables,
+    // lengths or plan (the caller's PKV_INPUTS_READY): a CTA reads its work item,
+    // stages its table and starts its first tile loads before waiting for the
+    // preceding kernel, then waits before it reads q, the new rows or the slots
+    // (and never loads early the chunk that receives the new token)
+    int early = 0;
 };
 
 // Sequences a call plans (sorts and compacts) at most; larger batches run the

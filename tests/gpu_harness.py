@@ -63,9 +63,11 @@ class DeviceStep:
             pkv.paged_kv_append(self.k_new, self.v_new, self.kc[l], self.vc[l], self.slot_mapping)
             self.decode(l)
 
-    def run_planned_fused(self):
+    def run_planned_fused(self, inputs_ready=False):
         """The benchmark's step: copy-on-write copies, one plan for the step, then per layer
-        the slot write fused into the decode launch (one new token per sequence)."""
+        the slot write fused into the decode launch (one new token per sequence); with
+        ``inputs_ready``, every layer after the first starts its tile loads early, as the
+        benchmark's step does."""
         wl, s = self.wl, self.wl.spec
         assert wl.num_tokens == s.num_seqs, "the fused call writes one token per sequence"
         if self.copy_pairs.shape[0]:
@@ -77,7 +79,8 @@ class DeviceStep:
             pkv.paged_kv_append_decode(self.out[l], self.q, self.k_new, self.v_new, self.kc[l], self.vc[l],
                                        self.slot_mapping, self.block_tables, self.seq_lens, wl.scale,
                                        max_seq_len=wl.max_seq_len, workspace=self.workspace,
-                                       partition_tokens=self.partition_tokens, planned=True, sum_seq_lens=total)
+                                       partition_tokens=self.partition_tokens, planned=True, sum_seq_lens=total,
+                                       inputs_ready=inputs_ready and l > 0)
 
     def decode(self, l=0):
         wl = self.wl

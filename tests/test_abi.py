@@ -83,13 +83,17 @@ def test_fused_and_verify_validation_rejects_before_launch(lib):
     null = ctypes.c_void_p(0)
     fake = ctypes.c_void_p(256)            # a non-null, aligned address that nothing dereferences
 
-    def fused(head_dim=128, dt=0, kv_dt=0, k_scale=null, v_scale=null, sum_lens=0, ptr=fake, slots=fake):
+    def fused(head_dim=128, dt=0, kv_dt=0, k_scale=null, v_scale=null, sum_lens=0, ptr=fake, slots=fake, planned=1):
         # out, q, k, v, key_cache, value_cache, slot_mapping, tables, width, lens, B, max_len, sum, Hq, Hkv, d, bs,
         # num_blocks, scale, dt, kv_dt, k_scale, v_scale, workspace, workspace_bytes, partition, planned, stream
         return lib.pkv_paged_kv_append_decode(ptr, ptr, ptr, ptr, ptr, ptr, slots, fake, 4, fake, 2, 10, sum_lens, 8, 2,
-                                              head_dim, 16, 10, 1.0, dt, kv_dt, k_scale, v_scale, null, 0, 0, 1, null)
+                                              head_dim, 16, 10, 1.0, dt, kv_dt, k_scale, v_scale, null, 0, 0, planned,
+                                              null)
 
     assert fused(sum_lens=-1) == pkv.PKV_ERR_INVALID
+    # planned: 0, PKV_PLANNED (1) or PKV_PLANNED | PKV_INPUTS_READY (3); inputs-ready alone or other bits refused
+    for bad in (pkv.INPUTS_READY, 4, 5, 7, -1):
+        assert fused(planned=bad) == pkv.PKV_ERR_INVALID and b"planned" in lib.pkv_last_error()
     assert fused(kv_dt=1) == pkv.PKV_ERR_INVALID and b"kv_dt" in lib.pkv_last_error()   # 16-bit pools: kv_dt == dt
     assert fused(kv_dt=2) == pkv.PKV_ERR_INVALID                                          # E4M3 without scales
     assert fused(head_dim=96) == pkv.PKV_ERR_UNSUPPORTED

@@ -135,6 +135,55 @@ def test_fused_matches_oracle_and_separate_calls(case, partition_tokens, planned
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16)), "fused and separate calls differ"
 
 
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+@pytest.mark.parametrize("case", [0, 1, 2, 3, 4])
+def test_inputs_ready_layers_match(case, partition_tokens):
+    """One plan, then four layers' fused calls, every layer after the first with inputs_ready
+    (its work item, table slice and first tiles are read before it waits for the preceding
+    launch): the pools bit-exact against the oracle's append, the outputs bit-identical to the
+    same calls without the flag and within tolerance of the oracle.  Case 0's short sequences
+    put the new token in the first chunks (loaded only after its slot is written); case 3's 12
+    query heads per KV head give two CTAs per KV head writing the same slot; case 4 (E4M3)
+    accepts the flag and runs as without it."""
+    wl = build(case, 900 + case)
+    s = wl.spec
+    x = Inputs(wl)
+    layers = 4
+    rk, rv, ref = oracle_step(wl)
+    outs = {}
+    for ready in (False, True):
+        ws = pkv.alloc_workspace(s.num_seqs, s.num_heads, s.num_kv_heads, s.head_dim, wl.max_seq_len,
+                                 partition_tokens)
+        pools = [device_pools(wl) for _ in range(layers)]
+        pkv.decode_plan(ws, x.tables, x.lens, s.num_heads, pools[0][0], wl.max_seq_len, partition_tokens,
+                        sum_seq_lens=x.total)
+        outs[ready] = []
+        for l, (kc, vc) in enumerate(pools):
+            out = torch.full_like(x.q, float("nan"))
+            pkv.paged_kv_append_decode(out, x.q, x.k, x.v, kc, vc, x.slots, x.tables, x.lens, wl.scale,
+                                       max_seq_len=wl.max_seq_len, workspace=ws, partition_tokens=partition_tokens,
+                                       planned=True, sum_seq_lens=x.total, k_scale=x.ks, v_scale=x.vs,
+                                       inputs_ready=ready and l > 0)
+            outs[ready].append(out)
+        torch.cuda.synchronize()
+        for kc, vc in pools:
+            assert np.array_equal(pool_bits(kc), rk) and np.array_equal(pool_bits(vc), rv)
+    for l in range(layers):
+        assert torch.equal(outs[True][l].view(torch.int16), outs[False][l].view(torch.int16)), f"layer {l}"
+        err = max_abs_err(outs[True][l], ref)
+        assert err <= TOL[s.dtype], f"layer {l}: max abs err {err}"
+
+
+def test_inputs_ready_needs_a_plan():
+    wl = build(0, 950)
+    x = Inputs(wl)
+    kc, vc = device_pools(wl)
+    out = torch.empty_like(x.q)
+    with pytest.raises(ValueError):
+        pkv.paged_kv_append_decode(out, x.q, x.k, x.v, kc, vc, x.slots, x.tables, x.lens, wl.scale,
+                                   max_seq_len=wl.max_seq_len, inputs_ready=True)
+
+
 @pytest.mark.parametrize("case", [0, 4])
 def test_plan_once_fused_layers(case):
     """One plan, then the fused call on several layers' pools (the tickets reset between runs)."""

@@ -211,13 +211,13 @@ def test_full_size_workload(name, mode):
     assert err <= TOL[wl.spec.dtype], f"{name}: max abs err {err}"
 
 
-@pytest.mark.parametrize("mode", ["separate", "fused"])
+@pytest.mark.parametrize("mode", ["separate", "fused", "fused_inputs_ready"])
 def test_full_size_80_layer_step(mode):
     wl = W.build(W.SPECS["llama2_70b_step"], values="none")
     step = DeviceStep(wl, pools="device")
     check_layers = (0, 41, 79)
     pre = {l: (to_bits(step.kc[l]), to_bits(step.vc[l])) for l in check_layers}
-    step.run() if mode == "separate" else step.run_planned_fused()
+    step.run() if mode == "separate" else step.run_planned_fused(inputs_ready=mode == "fused_inputs_ready")
     torch.cuda.synchronize()
     for l in range(80):
         assert torch.isfinite(step.out[l]).all(), f"layer {l}"
