@@ -85,10 +85,11 @@ __device__ __forceinline__ uint32_t q_as_f16x2<__nv_bfloat16>(uint32_t x) {
 // UNITS: the work list may hold shared-prefix units (16-bit decode only; the
 // host launches this form when the plan may make them).
 // Register caps: an SM's four sub-partitions each hold a quarter of the register
-// file (16384) and take the resident warps in turn, so the 5-warp CTAs fit 3 to an
-// SM (head_dim 128, 16-bit) at 128 registers, 4 (E4M3) at 96, 6 (head_dim 64) at 64.
+// file (16384) and take the resident warps in turn, so the 5-warp CTAs that shared
+// memory allows 3 to an SM (head_dim 128, 16-bit or E4M3) fit at 128 registers, and
+// the 6 of head_dim 64 at 64.
 template <typename T, int D, int CW, int STAGES, bool MQ, bool KV8 = false, bool UNITS = false>
-__global__ void __maxnreg__(KV8 ? 96 : D == 64 ? 64 : 128) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __maxnreg__(D == 64 ? 64 : 128) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                      const __grid_constant__ CUtensorMap tmv,
                                                                      const DecodeArgs a) {
     static_assert(!KV8 || D == 128, "E4M3 pools: head_dim 128");

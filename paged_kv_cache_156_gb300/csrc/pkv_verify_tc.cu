@@ -690,62 +690,114 @@ __global__ void __launch_bounds__(TcGeo<D, M>::kThreads, 2) verify_tc_kernel(con
     }
     if (!epi_sync()) return;
     if (!*merge_flag) return;
-    // every softmax thread merges: 128 / M threads a row, D * M / 128 columns each, 16 columns
-    // and four partitions' loads in flight at a time (partitions summed in order)
+    // every softmax thread merges: 128 / M threads a row, D * M / 128 columns each
     constexpr int kTpr = TG::kSoftmaxThreads / M;   // threads per row
     constexpr int kCols = D / kTpr;                 // columns per thread
-    const int mrow = rg * TG::kRows + static_cast<int>(threadIdx.x) / kTpr;
-    if (mrow >= R) return;
+    const int mr = static_cast<int>(threadIdx.x) / kTpr;
+    const int mrow = rg * TG::kRows + mr;
     const int cb = (static_cast<int>(threadIdx.x) % kTpr) * kCols;
+    // Partitions that fit the (now idle) K/V ring: all of them copied in at once (every
+    // thread's 16-byte copies in flight together), then summed from shared memory; more
+    // partitions than fit: straight from global memory, four partitions' loads at a time.
+    constexpr int kPartBytes = M * D * 4;
+    constexpr int kFit = static_cast<int>(TG::kRing / kPartBytes);
+    static_assert(kFit >= 1, "one partition's rows fit the ring");
     const float2* ml = a.ws_ml + (prow0 + mrow) * a.max_parts;
     const float* wo = a.ws_o + (prow0 + mrow) * a.max_parts * D;
+    float* part_sm = reinterpret_cast<float*>(smem);
+    const bool staged = nparts <= kFit;
+    if (staged) {
+        constexpr int kVec = D / 4;                 // 16-byte pieces of a row
+        const int pieces = nparts * M * kVec;
+        for (int i = threadIdx.x; i < pieces; i += TG::kSoftmaxThreads) {
+            const int j = i / (M * kVec), rem = i - j * (M * kVec);
+            const int r = rem / kVec, c4 = rem - r * kVec;
+            const int grow = rg * TG::kRows + r;
+            if (grow >= R) continue;
+            const float* src = a.ws_o + ((prow0 + grow) * a.max_parts + j) * D + 4 * c4;
+            const uint32_t dst = smem_u32(part_sm + (static_cast<size_t>(j) * M + r) * D + 4 * c4);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    // the rows' (maximum, sum) pairs, up to 8 at once
+    constexpr int kMl = 8;
+    static_assert(kFit <= kMl, "staged partitions have their weights in registers");
+    float2 e[kMl];
+#pragma unroll
+    for (int p = 0; p < kMl; ++p)
+        e[p] = (p < nparts && mrow < R) ? __ldcg(ml + p) : make_float2(-INFINITY, 0.0f);
     float mmax = -INFINITY;
-    for (int p = 0; p < nparts; ++p) mmax = fmaxf(mmax, __ldcg(ml + p).x);
+#pragma unroll
+    for (int p = 0; p < kMl; ++p) mmax = fmaxf(mmax, e[p].x);
+    for (int p = kMl; p < nparts && mrow < R; ++p) mmax = fmaxf(mmax, __ldcg(ml + p).x);
     float den = 0.0f;
-    for (int p = 0; p < nparts; ++p) {
-        const float2 e = __ldcg(ml + p);
-        den += e.x == -INFINITY ? 0.0f : fast_exp2(e.x - mmax) * e.y;
+#pragma unroll
+    for (int p = 0; p < kMl; ++p) den += e[p].x == -INFINITY ? 0.0f : fast_exp2(e[p].x - mmax) * e[p].y;
+    for (int p = kMl; p < nparts && mrow < R; ++p) {
+        const float2 x = __ldcg(ml + p);
+        den += x.x == -INFINITY ? 0.0f : fast_exp2(x.x - mmax) * x.y;
     }
     const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+    if (staged) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (!epi_sync()) return;                    // every thread's pieces landed
+    }
+    if (mrow >= R) return;
     T* orow = out + tc_row_offset(a, s, kvh, mrow) * D;
 #pragma unroll 1
     for (int c0 = cb; c0 < cb + kCols; c0 += 16) {
         float num[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) num[j] = 0.0f;
-#pragma unroll 1
-        for (int p0 = 0; p0 < nparts; p0 += 4) {
-            float w[4];
-            float4 v[4][4];
+        for (int jj = 0; jj < 16; ++jj) num[jj] = 0.0f;
+        if (staged) {
+            for (int p = 0; p < nparts; ++p) {
+                const float w = p < kMl ? (e[p].x == -INFINITY ? 0.0f : fast_exp2(e[p].x - mmax)) : 0.0f;
+                const float4* src = reinterpret_cast<const float4*>(part_sm + (static_cast<size_t>(p) * M + mr) * D + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int p = p0 + q;
-                w[q] = 0.0f;
-                if (p < nparts) {
-                    const float2 e = __ldcg(ml + p);
-                    w[q] = e.x == -INFINITY ? 0.0f : fast_exp2(e.x - mmax);
-                    const float4* src = reinterpret_cast<const float4*>(wo + static_cast<int64_t>(p) * D + c0);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[q][j] = __ldcg(src + j);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[q][j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 v = src[jj];
+                    num[4 * jj] += w * v.x;
+                    num[4 * jj + 1] += w * v.y;
+                    num[4 * jj + 2] += w * v.z;
+                    num[4 * jj + 3] += w * v.w;
                 }
             }
+        } else {
+#pragma unroll 1
+            for (int p0 = 0; p0 < nparts; p0 += 4) {
+                float w[4];
+                float4 v[4][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 4; ++q) {
+                    const int p = p0 + q;
+                    w[q] = 0.0f;
+                    if (p < nparts) {
+                        const float2 x = __ldcg(ml + p);
+                        w[q] = x.x == -INFINITY ? 0.0f : fast_exp2(x.x - mmax);
+                        const float4* src = reinterpret_cast<const float4*>(wo + static_cast<int64_t>(p) * D + c0);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    num[4 * j] += w[q] * v[q][j].x;
-                    num[4 * j + 1] += w[q] * v[q][j].y;
-                    num[4 * j + 2] += w[q] * v[q][j].z;
-                    num[4 * j + 3] += w[q] * v[q][j].w;
+                        for (int jj = 0; jj < 4; ++jj) v[q][jj] = __ldcg(src + jj);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) v[q][jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        num[4 * jj] += w[q] * v[q][jj].x;
+                        num[4 * jj + 1] += w[q] * v[q][jj].y;
+                        num[4 * jj + 2] += w[q] * v[q][jj].z;
+                        num[4 * jj + 3] += w[q] * v[q][jj].w;
+                    }
                 }
             }
         }
         uint32_t wv[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) wv[j] = pack2<T>(num[2 * j] * inv, num[2 * j + 1] * inv);
+        for (int jj = 0; jj < 8; ++jj) wv[jj] = pack2<T>(num[2 * jj] * inv, num[2 * jj + 1] * inv);
         uint4* dst = reinterpret_cast<uint4*>(orow + c0);
         dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
