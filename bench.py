@@ -39,7 +39,6 @@ import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
-NOMINAL_HBM_GBS = 7900.0       # GB300 HBM3e nominal bandwidth: context beside the measured peak
 MIN_DECODE_EVENTS = 50         # CUDA-event samples behind the decode launch's median
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak); decode tokens/s"
 
@@ -141,22 +140,23 @@ def decode_source_hash() -> str:
 
 def verify_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("pkv_verify.cu", "pkv_decode_common.cuh", "pkv_device.cuh"):
+    for name in ("pkv_verify_tc.cu", "pkv_tcgen05.cuh", "pkv_decode_common.cuh", "pkv_decode_plan.cu", "pkv_device.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_156_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_verify_traffic(workload: str, num_queries: int):
+def profiled_verify_traffic(workload: str, num_queries: int, fp8: bool = False):
     """Per-launch DRAM bytes of the verify kernel from the committed ncu summary for
-    this workload and query count, or None (no summary, or the sources changed)."""
+    this workload and query count, or None (no summary, or the sources changed).  An
+    E4M3 pool's verify runs the decode kernel's multi-query form: its sources decide."""
     path = os.path.join(ROOT, "profiles", f"verify_{workload}_nq{num_queries}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    m_h = re.search(r"verify_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m_t or not m_h or m_h.group(1) != verify_source_hash():
+    m_h = re.search(r"(?:verify|decode)_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != (decode_source_hash() if fp8 else verify_source_hash()):
         return None
     return int(m_t.group(1))
 
@@ -574,7 +574,6 @@ def run_pkv(args, rank, world, local):
                                                 "; the step's one plan kernel is outside this timing, inside value)"),
                      "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(dec_gbs / NOMINAL_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 5),
                      "launch_events": len(ev_pairs), "launch_events_in_timed_region": n_timed_events},
         "cpu_baseline": cpu,
@@ -797,9 +796,8 @@ def run_verify(args, rank, world, local):
             "config": {"workload": spec.name, "num_queries": nq, "partition_tokens": part,
                        "l2": f"{replicas} rotating pool replicas"},
             "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "peak_kind": peak_kind,
-                         "unit": "GB/s", "frac": round(gbs / world / peak, 4), "nominal_peak": NOMINAL_HBM_GBS,
-                         "frac_of_nominal": round(gbs / world / NOMINAL_HBM_GBS, 4),
-                         "traffic": profiled_verify_traffic(spec.name, nq),
+                         "unit": "GB/s", "frac": round(gbs / world / peak, 4),
+                         "traffic": profiled_verify_traffic(spec.name, nq, spec.fp8),
                          "algorithmic_bytes_per_launch": int(nbytes)},
             "gpu_launches": 2 * args.steps}
 

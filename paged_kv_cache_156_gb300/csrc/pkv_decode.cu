@@ -162,7 +162,9 @@ __global__ void __maxnreg__(D == 64 ? 64 : 128) decode_kernel(const __grid_const
         Lp = -1;
     }
     const bool grouped = kUnits && un > 1;          // a shared-prefix unit (CTA-uniform)
-    const bool early = a.early && a.plan && !grouped && !MQ && !KV8;   // (CTA-uniform)
+    // (CTA-uniform; compiled only into the unit-free 16-bit decode form, the one whole-step
+    // batches without forks use)
+    const bool early = !kUnits && !MQ && !KV8 && a.early && a.plan && !grouped;
     if (a.early && !early) grid_dependency_wait();
     const int hg = hh % a.head_groups;
     const int kvh = hh / a.head_groups;
