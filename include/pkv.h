@@ -314,6 +314,10 @@ PKV_API pkv_status pkv_paged_kv_append_decode(void* out, const void* q, const vo
  *                 query token that sees no position gets a zero output)
  *   sum_seq_lens  the sum of seq_lens if known, else 0; it only sizes the
  *                 grid, as for pkv_paged_attention_decode_planned
+ * A KV head serves R = (num_heads / num_kv_heads) * num_queries query rows.
+ * R > 16: the tensor-core verify kernel (tcgen05), 64 rows per CTA when
+ * R <= 64, else 128 (head_groups = ceil(R / 128)), K/V streamed once per
+ * row group; R <= 16: the decode kernel's multi-query form, 8 rows per CTA.
  */
 PKV_API pkv_status pkv_paged_attention_verify(void* out, const void* q, const void* key_cache,
                                       const void* value_cache, const int32_t* block_tables,
@@ -367,8 +371,11 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, cons
  * over the low-precision K/V), with K and V as in
  * pkv_paged_attention_decode_fp8 and the causal mask of
  * pkv_paged_attention_verify.  q, out [num_seqs][num_queries][num_heads][128]
- * in dt (PKV_F16 or PKV_BF16).  Query rows are served 8 per CTA, so a KV
- * head with many rows streams its K/V once per 8 rows.
+ * in dt (PKV_F16 or PKV_BF16).  Query rows are served 8 per CTA (the decode
+ * kernel's multi-query form), so the CTAs of a KV head with many rows read
+ * the same tiles; they run side by side (row groups are adjacent in the
+ * grid), so L2 serves all but the first read, but each does the full
+ * per-position work: R rows cost R / 8 CTAs' worth of arithmetic.
  */
 PKV_API pkv_status pkv_paged_attention_verify_fp8(void* out, const void* q, const void* key_cache,
                                           const void* value_cache, const int32_t* block_tables,

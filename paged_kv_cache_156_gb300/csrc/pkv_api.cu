@@ -379,7 +379,7 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     a.qgroup = num_heads / num_kv_heads;
     a.num_queries = num_queries;
     a.group = a.qgroup * num_queries;
-    // more than kVerifyMinRows query rows per KV head: the verify kernel, 32 or 64 rows per CTA
+    // more than kVerifyMinRows query rows per KV head: the tensor-core verify kernel, 64 or 128 rows per CTA
     // (E4M3 pools: the decode kernel's multi-query form, 8 rows per CTA, for any row count)
     const bool verify_kernel = num_queries > 1 && a.group > pkv::kVerifyMinRows && !kv8;
     a.head_groups = verify_kernel ? (a.group + pkv::kVerifyTcRows - 1) / pkv::kVerifyTcRows : (a.group + 7) / 8;

@@ -183,15 +183,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmk, const CUt
                           int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
 cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t s);
 
-// The multi-query (verify) kernel for more than kVerifyMinRows query rows per
-// KV head: up to 64 rows per CTA (head_groups = ceil(rows / 64)).
+// More than kVerifyMinRows query rows per KV head (num_queries > 1, 16-bit pools):
+// the verify kernel on the tensor cores; fewer, and E4M3 pools: the decode
+// kernel's multi-query form, 8 rows per CTA.
 constexpr int kVerifyMinRows = 16;
-// Query rows one verify CTA serves for a KV head with `rows` rows: 32 (two warps
-// per 16-row tile) or 64 (one warp per tile).
-int verify_rows_per_cta(int rows);
-cudaError_t launch_verify(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int dtype,
-                          int head_dim, cudaStream_t s, DecodeMode mode = DecodeMode::kPlanAndRun);
-int verify_ctas_per_sm(int head_dim, int rows);   // rows: query rows per KV head
 
 // The verify kernel on the fifth-generation tensor cores (tcgen05): up to
 // kVerifyTcRows query rows per CTA (head_groups = ceil(rows / kVerifyTcRows));
