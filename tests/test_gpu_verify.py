@@ -3,10 +3,11 @@
 The last num_queries positions of each sequence are the query tokens' own K/V;
 query token i sees positions < L - num_queries + i + 1.  Cases cover query
 rows that fit one 8-row group and several, more than 16 rows per KV head (the
-rows-as-M kernel: up to 32 rows with two warps per 16-row tile, one and two
-64-row groups, partly filled warps), with and without the lengths' sum, one and
-several partitions, query tokens that see nothing in a late partition, an
-empty sequence, both head sizes and every block size.
+tensor-core kernel: M = 64 tiles partly and wholly filled, M = 128 tiles, two
+row groups per KV head), with and without the lengths' sum, one and several
+partitions (merged from shared memory or, past what the ring holds, from
+global memory), query tokens that see nothing in a late partition, an empty
+sequence, both head sizes and every block size.
 """
 import numpy as np
 import pytest
@@ -35,13 +36,19 @@ CASES = [
          lens=("fixed", (4, 1025, 700, 64, 65))),
     dict(num_heads=4, num_kv_heads=4, head_dim=64, block_size=32, dtype=W.F16, nq=3, lens=("fixed", (3, 17, 2000))),
     dict(num_heads=12, num_kv_heads=4, head_dim=128, block_size=16, dtype=W.BF16, nq=5, lens=("fixed", (130, 5, 513))),
-    # more than 16 rows per KV head: the rows-as-M verify kernel (64 rows per CTA)
+    # more than 16 rows per KV head: the tensor-core verify kernel (an M = 64 tile up to 64 rows)
     dict(num_heads=32, num_kv_heads=8, head_dim=128, block_size=16, dtype=W.BF16, nq=5,
          lens=("fixed", (5, 6, 64, 65, 1500, 3000))),
     dict(num_heads=16, num_kv_heads=2, head_dim=128, block_size=32, dtype=W.F16, nq=8, lens=("fixed", (8, 900, 77))),
     dict(num_heads=8, num_kv_heads=1, head_dim=64, block_size=8, dtype=W.BF16, nq=10, lens=("fixed", (10, 400, 1025))),
     dict(num_heads=64, num_kv_heads=8, head_dim=128, block_size=16, dtype=W.F16, nq=3, lens=("fixed", (0, 3, 2049, 700))),
-    # exactly 32 rows per KV head at head_dim 64: two warps share each 16-row tile
+    # 128 rows per KV head at head_dim 128 (the M = 128 tile), and 160 (two row groups, the second
+    # holding 32 rows)
+    dict(num_heads=64, num_kv_heads=8, head_dim=128, block_size=16, dtype=W.BF16, nq=16,
+         lens=("fixed", (16, 1500, 3000))),
+    dict(num_heads=32, num_kv_heads=4, head_dim=128, block_size=16, dtype=W.F16, nq=20,
+         lens=("fixed", (20, 700, 2100))),
+    # exactly 32 rows per KV head at head_dim 64 (an M = 64 tile, half of it empty rows)
     dict(num_heads=16, num_kv_heads=2, head_dim=64, block_size=16, dtype=W.BF16, nq=4,
          lens=("fixed", (4, 31, 33, 95, 97, 2100))),
 ]
