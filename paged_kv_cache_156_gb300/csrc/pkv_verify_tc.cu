@@ -9,38 +9,35 @@
 //
 // How.  A KV head serves R = (num_heads / num_kv_heads) * num_queries query
 // rows; one CTA serves M of them, M = 64 when R <= 64, else 128 (rows past R
-// are zero).  An M = 64 product keeps its rows in the first 16 TMEM lanes of
-// each warp's 32-lane quarter (rows 16 w .. 16 w + 15 in lanes 32 w ..), so
-// each softmax warp holds 16 rows in its first 16 lanes.  The K/V tiles
-// arrive by TMA, 128-byte swizzled, from the same work list as decode, in a
-// ring of six stages of 32 positions (a stage is freed as soon as its own
-// product is done, so most of the ring is always loading), and per stage:
-//   S = Q K^T      tcgen05.mma, M rows, N = 32 positions: A = Q held in
-//                  tensor memory (TMEM) as 16-bit pairs, B = the stage's K rows
-//                  (K-major, 128-byte swizzle), S in TMEM as fp32, two S
-//                  buffers in turn;
-//   softmax        one thread per row reads its 32 scores (tcgen05.ld),
-//                  masks positions past the partition and past its causal
-//                  limit, and keeps a running reference maximum that moves
-//                  only when a score exceeds it by more than 2^8 (then the
-//                  row's O and sum are rescaled in TMEM); it writes
-//                  P = 2^(s - ref) rounded to the input type into its half
-//                  of a 128-byte-swizzled shared-memory tile and adds the
-//                  rounded values to its sum;
-//   O += P V       tcgen05.mma, A = that P half (K-major), B = the stage's V
+// are zero), over one partition of one sequence from the same work list as
+// decode.  An M = 64 product keeps its rows in the first 16 TMEM lanes of each
+// warp's 32-lane quarter (rows 16 w .. 16 w + 15 in lanes 32 w ..).  The K/V
+// tiles arrive by TMA, 128-byte swizzled, into a ring of 32-position stages
+// laid out plane-major (plane, stage, position), so that the two stages of a
+// 64-position step sit side by side in every plane, and per step:
+//   S = Q K^T      tcgen05.mma, M rows x N = 64 positions: A = Q held in
+//                  tensor memory (TMEM) as 16-bit pairs, B = the step's K rows
+//                  (K-major, 128-byte swizzle), S in TMEM as fp32;
+//   softmax        M = 64: the 16x256b TMEM load shape gives each thread two
+//                  rows x 16 columns (all 32 lanes busy), the row maximum
+//                  reduced over the quad; M = 128: one row a thread.  Positions
+//                  past the partition and past the row's causal limit are
+//                  masked; a running reference maximum moves only when a score
+//                  exceeds it by more than 2^8 (then the rows' O and sums are
+//                  rescaled in TMEM); P = 2^(s - ref) rounded to the input type
+//                  goes to one of two 128-byte-swizzled P buffers;
+//   O += P V       tcgen05.mma, A = that P buffer (K-major), B = the step's V
 //                  read as an MN-major operand (its 64-element column blocks
-//                  one 4 KB plane apart), O in TMEM as fp32.
-// One thread issues the MMAs.  Once a half's P is written it issues that
-// half's O += P V and, right behind it, the S of the half after next into
-// the buffer just read, and commits both to that buffer's mbarrier: when
-// that S lands, the product that read the same P half is done too.  The
-// softmax threads meanwhile work on the other buffer's half, so the tensor
-// core and the softmax overlap.  A producer warp streams the tiles (its lane 0 reads
-// each stage's block ids from the table one stage ahead); TMEM holds Q, the
-// two S buffers and O (256 columns), the shared memory the K/V ring (96 KB)
-// and P, so two CTAs share an SM.
-// Split partitions write (reference max, sum, unnormalised O) per row and the
-// CTA that takes the last ticket merges them (split-K), as decode does.
+//                  one plane apart), O in TMEM as fp32.
+// The S products and the O products are issued by one thread each (warps 6 and
+// 5), so the next step's S never waits behind this step's O product; a stage is
+// refilled as soon as the O product that read it is done.  A producer warp
+// streams the tiles (its lane 0 reads each stage's block ids one stage ahead).
+// TMEM holds Q, S and O (256 columns), the shared memory the ring (96 KB at
+// M = 64) and P, so two CTAs share an SM.
+// Split partitions write (reference max, sum, unnormalised O) per row; the CTA
+// that takes the last ticket merges them (split-K), from shared memory when the
+// partitions' rows fit the idle ring, else from global memory.
 // Every wait is bounded in wall time; a CTA that gives up raises the error
 // word, waits (bounded) for its own MMAs and frees its TMEM.
 #include <algorithm>
