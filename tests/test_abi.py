@@ -30,6 +30,17 @@ def test_header_declares_the_binding_symbols():
     assert declared_symbols() == sorted(pkv.ABI_SYMBOLS)
 
 
+def test_header_constants_match_the_binding():
+    """The values the header defines and the binding passes (PKV_PLANNED, PKV_INPUTS_READY,
+    PKV_PLAN_MAX_SEQS) agree."""
+    text = open(HEADER).read()
+    defined = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(PKV_\w+)\s+(\d+)\s*$", text, re.M)}
+    assert defined["PKV_PLANNED"] == pkv.PLANNED
+    assert defined["PKV_INPUTS_READY"] == pkv.INPUTS_READY
+    assert defined["PKV_PLAN_MAX_SEQS"] == pkv.PLAN_MAX_SEQS
+    assert pkv.PLANNED & pkv.INPUTS_READY == 0
+
+
 def test_every_declared_symbol_is_exported(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\sT\s(pkv_\w+)$", out, re.M))
