@@ -77,18 +77,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete.  Returns
-// false (and never blocks longer than kWaitLimitNs) if it does not.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 // ---------------------------------------------------------------- TMA
 // 4-D tiled load into shared memory, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
@@ -111,23 +99,13 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-// 4-byte asynchronous global -> shared copy (completion tracked per thread by
-// commit groups: cp_async_commit / cp_async_wait_all).
-__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
+// 16-byte asynchronous global -> shared copy through L2 only (completion
+// tracked per thread by commit groups: cp_async_commit / cp_async_wait_all).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// Contiguous global -> shared bulk copy (16-byte aligned addresses, size a
-// multiple of 16), completion counted on `bar` (bytes).
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;

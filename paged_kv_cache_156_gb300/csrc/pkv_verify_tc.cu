@@ -713,9 +713,9 @@ __global__ void __launch_bounds__(TcGeo<D, M>::kThreads, 2) verify_tc_kernel(con
             if (grow >= R) continue;
             const float* src = a.ws_o + ((prow0 + grow) * a.max_parts + j) * D + 4 * c4;
             const uint32_t dst = smem_u32(part_sm + (static_cast<size_t>(j) * M + r) * D + 4 * c4);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+            cp_async_16(dst, src);
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        cp_async_commit();
     }
     // the rows' (maximum, sum) pairs, up to 8 at once
     constexpr int kMl = 8;
@@ -737,7 +737,7 @@ __global__ void __launch_bounds__(TcGeo<D, M>::kThreads, 2) verify_tc_kernel(con
     }
     const float inv = den > 0.0f ? 1.0f / den : 0.0f;
     if (staged) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        cp_async_wait_all();
         if (!epi_sync()) return;                    // every thread's pieces landed
     }
     if (mrow >= R) return;
