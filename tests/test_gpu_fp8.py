@@ -185,6 +185,37 @@ def test_verify_fp8_matches_oracle(case, partition_tokens):
     assert err <= TOL[s.dtype], f"max abs err {err}"
 
 
+@pytest.mark.parametrize("nq", [4, 8])
+def test_full_size_verify_fp8(nq):
+    """The benchmarked E4M3 verify launches (the 8B-shaped batch, 16 and 32 rows per KV head, the
+    benchmark's workspace and lengths' sum): every output of every sequence against the oracle."""
+    wl = W.build(W.SPECS["llama3_8b_fp8"], values="none")
+    s = wl.spec
+    assert int(wl.seq_lens.min()) >= nq
+    dk, dv = W.device_pools(wl, 0, "cuda")
+    kc, vc = dk.cpu().numpy().copy(), dv.cpu().numpy().copy()     # the generator's pools, before the step
+    ks, vs = wl.k_scales[0], wl.v_scales[0]
+    pkv.paged_kv_append_fp8(to_dev(wl.k_new, s.dtype), to_dev(wl.v_new, s.dtype), dk, dv, cuda_of(wl.slot_mapping),
+                            f32(ks), f32(vs))
+    rng = np.random.default_rng(950 + nq)
+    q = W.normal_bits(rng, (s.num_seqs, nq, s.num_heads, s.head_dim), s.dtype)
+    qd = to_dev(q, s.dtype)
+    out = torch.full_like(qd, float("nan"))
+    ws = pkv.alloc_workspace(s.num_seqs, s.num_heads * nq, s.num_kv_heads, s.head_dim, wl.max_seq_len, 0, "cuda")
+    pkv.paged_attention_verify(out, qd, dk, dv, cuda_of(wl.block_tables), cuda_of(wl.seq_lens), wl.scale,
+                               max_seq_len=wl.max_seq_len, workspace=ws, sum_seq_lens=int(wl.seq_lens.sum()),
+                               k_scale=f32(ks), v_scale=f32(vs))
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    oracle.append_fp8_ref(kc, vc, wl.k_new, wl.v_new, wl.slot_mapping, ks, vs, s.dtype)
+    ref = oracle.verify_attention_fp8_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype,
+                                          ks, vs)
+    err = max_abs_err(out, ref)
+    print(f"llama3_8b_fp8 verify nq={nq}: max abs err {err:.3g} over all {s.num_seqs} sequences x {nq} queries x "
+          f"{s.num_heads} heads")
+    assert err <= TOL[s.dtype], f"max abs err {err}"
+
+
 def test_verify_fp8_one_query_is_the_decode_call():
     wl = W.build(W.small_spec(num_seqs=5, num_heads=32, num_kv_heads=8, head_dim=128, dtype=W.BF16, seed=860,
                               kv_dtype=W.E4M3, lens=("fixed", (900, 33, 2049, 1, 4000))))

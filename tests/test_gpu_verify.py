@@ -16,7 +16,7 @@ import torch
 import oracle
 import paged_kv_cache_156_gb300 as pkv
 import workloads as W
-from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_caches_after_step, to_dev
+from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_caches_after_step, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -77,6 +77,39 @@ def test_verify_matches_oracle(case, partition_tokens, with_sum):
     ref = oracle.verify_attention_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
     assert torch.isfinite(out).all()
     err = max_abs_err(out, ref)
+    assert err <= TOL[s.dtype], f"max abs err {err}"
+
+
+# The benchmarked verify launches at full size (their workloads, query counts, workspace and
+# lengths' sum): the 70B-shaped mixed batch at 32, 64 and 128 rows per KV head (tensor-core
+# tiles of M = 64 half and wholly filled, then M = 128) and the 8B-shaped batch at 32 and 64 rows.
+FULL = [("llama2_70b_mixed_bs16", 4), ("llama2_70b_mixed_bs16", 8), ("llama2_70b_mixed_bs16", 16),
+        ("llama3_8b", 8), ("llama3_8b", 16)]
+
+
+@pytest.mark.parametrize("name,nq", FULL)
+def test_full_size_verify(name, nq):
+    """Every output of every sequence against the oracle."""
+    wl = W.build(W.SPECS[name], values="none")
+    s = wl.spec
+    assert len(wl.copy_pairs) == 0 and int(wl.seq_lens.min()) >= nq   # the query tokens' own slots exist
+    step = DeviceStep(wl, pools="device")
+    pre_k, pre_v = to_bits(step.kc[0]), to_bits(step.vc[0])
+    pkv.paged_kv_append(step.k_new, step.v_new, step.kc[0], step.vc[0], step.slot_mapping)
+    rng = np.random.default_rng(900 + nq)
+    q = W.normal_bits(rng, (s.num_seqs, nq, s.num_heads, s.head_dim), s.dtype)
+    qd = to_dev(q, s.dtype)
+    out = torch.full_like(qd, float("nan"))
+    ws = pkv.alloc_workspace(s.num_seqs, s.num_heads * nq, s.num_kv_heads, s.head_dim, wl.max_seq_len, 0, "cuda")
+    pkv.paged_attention_verify(out, qd, step.kc[0], step.vc[0], step.block_tables, step.seq_lens, wl.scale,
+                               max_seq_len=wl.max_seq_len, workspace=ws, sum_seq_lens=int(wl.seq_lens.sum()))
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    kc, vc = oracle_caches_after_step(wl, pre_k, pre_v)
+    ref = oracle.verify_attention_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
+    err = max_abs_err(out, ref)
+    print(f"{name} verify nq={nq}: max abs err {err:.3g} over all {s.num_seqs} sequences x {nq} queries x "
+          f"{s.num_heads} heads")
     assert err <= TOL[s.dtype], f"max abs err {err}"
 
 
