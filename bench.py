@@ -357,11 +357,19 @@ def run_pkv(args, rank, world, local):
 
     total_len = int(wl.seq_lens.sum())             # the scheduler knows it; it sizes the decode grid
     ev_pairs = []
+    copy_ev = []                                    # copy-on-write copies, timed apart from the decode
 
     def step(i, timed):
         kcs, vcs = pools[i % replicas]
         if len(wl.copy_pairs):
+            if timed:
+                ca = torch.cuda.Event(enable_timing=True)
+                ca.record()
             pkv.copy_blocks(kcs, vcs, pairs)
+            if timed:
+                cb = torch.cuda.Event(enable_timing=True)
+                cb.record()
+                copy_ev.append((ca, cb))
         if fused:
             pkv.decode_plan(ws, tables, lens, spec.num_heads, kcs[0], wl.max_seq_len, args.partition_tokens,
                             sum_seq_lens=total_len)
@@ -439,6 +447,13 @@ def run_pkv(args, rank, world, local):
     kernel_bytes = nbytes["decode_unique"] + (nbytes["append"] if fused else 0)
     dec_gbs = kernel_bytes / (dec_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
+    copy = None
+    if copy_ev:                                     # the step's copy_blocks launch on its own
+        copy_ms = float(np.median([a.elapsed_time(b) for a, b in copy_ev]))
+        copy = {"kernel": "copy_blocks_kernel", "pairs": int(len(wl.copy_pairs)), "layers": spec.num_layers,
+                "algorithmic_bytes_per_launch": nbytes["copy"], "avg_launch_ms": round(copy_ms, 5),
+                "achieved": round(nbytes["copy"] / (copy_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "frac": round(nbytes["copy"] / (copy_ms / 1e3) / 1e9 / peak, 4), "launch_events": len(copy_ev)}
 
     # ---- end to end: inputs from pinned host memory, outputs read back, every step
     def measure_e2e(use_graph):
@@ -576,6 +591,7 @@ def run_pkv(args, rank, world, local):
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": round(dec_ms, 5),
                      "launch_events": len(ev_pairs), "launch_events_in_timed_region": n_timed_events},
+        "copy_blocks": copy,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_eager": e2e_eager,

@@ -104,6 +104,11 @@ def oracle_attention(wl: W.Workload, kc: np.ndarray, vc: np.ndarray, seqs=None) 
                                 wl.spec.num_kv_heads, wl.spec.dtype)
 
 
+def mean_abs_err(gpu_out: torch.Tensor, ref: np.ndarray) -> float:
+    g = gpu_out.float().cpu().numpy().astype(np.float64)
+    return float(np.mean(np.abs(g - ref))) if g.size else 0.0
+
+
 def max_abs_err(gpu_out: torch.Tensor, ref: np.ndarray, seqs=None) -> float:
     g = gpu_out.float().cpu().numpy().astype(np.float64)
     if seqs is not None:

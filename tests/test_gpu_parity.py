@@ -13,7 +13,8 @@ import torch
 import oracle
 import paged_kv_cache_156_gb300 as pkv
 import workloads as W
-from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_attention, oracle_caches_after_step, to_bits, to_dev
+from gpu_harness import (TOL, DeviceStep, max_abs_err, mean_abs_err, oracle_attention, oracle_caches_after_step, to_bits,
+                         to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -207,7 +208,8 @@ def test_full_size_workload(name, mode):
     assert torch.isfinite(step.out[0]).all()
     ref = oracle_attention(wl, kc, vc)              # every sequence, every head
     err = max_abs_err(step.out[0], ref)
-    print(f"{name} ({mode}): max abs err {err:.3g} over all {s.num_seqs} sequences x {s.num_heads} heads")
+    print(f"{name} ({mode}): max abs err {err:.3g}, mean {mean_abs_err(step.out[0], ref):.3g} over all "
+          f"{s.num_seqs} sequences x {s.num_heads} heads")
     assert err <= TOL[wl.spec.dtype], f"{name}: max abs err {err}"
 
 
@@ -226,7 +228,8 @@ def test_full_size_80_layer_step(mode):
         assert np.array_equal(to_bits(step.kc[l]), kc) and np.array_equal(to_bits(step.vc[l]), vc)
         ref = oracle_attention(wl, kc, vc)          # all 16 sequences, every head
         err = max_abs_err(step.out[l], ref)
-        print(f"llama2_70b_step ({mode}) layer {l}: max abs err {err:.3g} over all sequences x heads")
+        print(f"llama2_70b_step ({mode}) layer {l}: max abs err {err:.3g}, mean {mean_abs_err(step.out[l], ref):.3g} "
+              f"over all sequences x heads")
         assert err <= TOL[W.BF16], f"layer {l}: {err}"
 
 

@@ -16,7 +16,7 @@ import torch
 import oracle
 import paged_kv_cache_156_gb300 as pkv
 import workloads as W
-from gpu_harness import TOL, DeviceStep, max_abs_err, oracle_caches_after_step, to_bits, to_dev
+from gpu_harness import TOL, DeviceStep, max_abs_err, mean_abs_err, oracle_caches_after_step, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -108,7 +108,8 @@ def test_full_size_verify(name, nq):
     kc, vc = oracle_caches_after_step(wl, pre_k, pre_v)
     ref = oracle.verify_attention_ref(q, kc, vc, wl.block_tables, wl.seq_lens, wl.scale, s.num_kv_heads, s.dtype)
     err = max_abs_err(out, ref)
-    print(f"{name} verify nq={nq}: max abs err {err:.3g} over all {s.num_seqs} sequences x {nq} queries x "
+    print(f"{name} verify nq={nq}: max abs err {err:.3g}, mean {mean_abs_err(out, ref):.3g} over all "
+          f"{s.num_seqs} sequences x {nq} queries x "
           f"{s.num_heads} heads")
     assert err <= TOL[s.dtype], f"max abs err {err}"
 
