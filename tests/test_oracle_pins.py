@@ -644,11 +644,63 @@ def _merge_wrong_weight(ms, ls, os):
     return sum(wi * oi for wi, oi in zip(w, os)) / float(np.dot(w, ls))
 
 
+def _verify_with_limit(limit, head_map=lambda h, G, Hkv: h // G):
+    """verify_attention_ref with query token i seeing positions t < limit(L, nq, i)."""
+    def run(q, kc, vc, tables, lens, scale, Hkv, dtype):
+        B, nq, Hq, d = q.shape
+        G = Hq // Hkv
+        out = np.zeros((B, nq, Hq, d))
+        for s in range(B):
+            L = int(lens[s])
+            for h in range(Hq):
+                g = head_map(h, G, Hkv)
+                K = oracle.gather_sequence(kc, tables[s], L, g, dtype)
+                V = oracle.gather_sequence(vc, tables[s], L, g, dtype)
+                for i in range(nq):
+                    vis = min(L, limit(L, nq, i))
+                    if L <= 0 or vis <= 0:
+                        continue
+                    out[s, i, h] = oracle.softmax_attention(oracle.decode_bits(q[s, i, h], dtype), K[:vis], V[:vis],
+                                                            scale)
+        return out
+    return run
+
+
+def _verify_excludes_itself(*a):
+    return _verify_with_limit(lambda L, nq, i: L - nq + i)(*a)
+
+
+def _verify_sees_next_token(*a):
+    return _verify_with_limit(lambda L, nq, i: L - nq + i + 2)(*a)
+
+
+def _verify_reversed_queries(*a):
+    return _verify_with_limit(lambda L, nq, i: L - i)(*a)
+
+
+def _verify_no_causal_mask(*a):
+    return _verify_with_limit(lambda L, nq, i: L)(*a)
+
+
+def _verify_mod_mapping(*a):
+    return _verify_with_limit(lambda L, nq, i: L - nq + i + 1, head_map=lambda h, G, Hkv: h % Hkv)(*a)
+
+
 MUTANTS = [("softmax_attention", _softmax_no_scale), ("softmax_attention", _softmax_kv_swapped),
            ("softmax_attention", _softmax_unnormalised), ("softmax_attention", _softmax_sign),
            ("softmax_attention", _softmax_no_max), ("gather_sequence", _gather_ignores_table),
            ("gather_sequence", _gather_off_by_one), ("attention_ref", _attention_mod_mapping),
-           ("merge_partials", _merge_wrong_weight)]
+           ("merge_partials", _merge_wrong_weight), ("verify_attention_ref", _verify_excludes_itself),
+           ("verify_attention_ref", _verify_sees_next_token), ("verify_attention_ref", _verify_reversed_queries),
+           ("verify_attention_ref", _verify_no_causal_mask), ("verify_attention_ref", _verify_mod_mapping)]
+
+
+def test_verify_mutant_scaffold_unmutated_passes_every_pin(monkeypatch):
+    """The scaffold the verify mutants share, with the right causal limit and GQA mapping,
+    passes every pin: what the pins catch in the mutants is the planted change."""
+    monkeypatch.setattr(oracle, "verify_attention_ref", _verify_with_limit(lambda L, nq, i: L - nq + i + 1))
+    for pin in PINS:
+        pin()
 
 
 @pytest.mark.parametrize("name,mutant", MUTANTS, ids=lambda x: getattr(x, "__name__", x))
