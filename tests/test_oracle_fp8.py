@@ -203,9 +203,56 @@ def _attention_fp8_k_scale_per_query_head(q, kc, vc, tables, lens, scale, Hkv, q
     return out
 
 
+def _verify_fp8_with(limit=lambda L, nq, i: L - nq + i + 1, k_scale_of=lambda ks, h, g: ks[g],
+                     v_scale_of=lambda vs, g: vs[g]):
+    """verify_attention_fp8_ref with the causal limit and the scale lookups as parameters."""
+    def run(q, kc, vc, tables, lens, scale, Hkv, q_dtype, ks, vs):
+        B, nq, Hq, d = q.shape
+        G = Hq // Hkv
+        ks = np.asarray(ks, np.float32).astype(np.float64)
+        vs = np.asarray(vs, np.float32).astype(np.float64)
+        out = np.zeros((B, nq, Hq, d))
+        for s in range(B):
+            L = int(lens[s])
+            for h in range(Hq):
+                g = h // G
+                K = oracle.gather_sequence(kc, tables[s], L, g, oracle.E4M3) * k_scale_of(ks, h, g)
+                V = oracle.gather_sequence(vc, tables[s], L, g, oracle.E4M3) * v_scale_of(vs, g)
+                for i in range(nq):
+                    vis = min(L, limit(L, nq, i))
+                    if L <= 0 or vis <= 0:
+                        continue
+                    out[s, i, h] = oracle.softmax_attention(oracle.decode_bits(q[s, i, h], q_dtype), K[:vis],
+                                                            V[:vis], scale)
+        return out
+    return run
+
+
+def _verify_fp8_no_v_scale(*a):
+    return _verify_fp8_with(v_scale_of=lambda vs, g: 1.0)(*a)
+
+
+def _verify_fp8_k_scale_per_query_head(*a):
+    return _verify_fp8_with(k_scale_of=lambda ks, h, g: ks[h % len(ks)])(*a)
+
+
+def _verify_fp8_excludes_itself(*a):
+    return _verify_fp8_with(limit=lambda L, nq, i: L - nq + i)(*a)
+
+
+def test_verify_fp8_mutant_scaffold_unmutated_passes_every_pin(monkeypatch):
+    """The verify mutants' scaffold with the right limit and scales passes every pin."""
+    monkeypatch.setattr(oracle, "verify_attention_fp8_ref", _verify_fp8_with())
+    for pin in FP8_PINS:
+        pin()
+
+
 MUTANTS = [("e4m3_value", _value_bias_8), ("e4m3_quantize", _quantize_ties_up),
            ("e4m3_quantize", _quantize_truncates), ("attention_fp8_ref", _attention_fp8_no_v_scale),
-           ("attention_fp8_ref", _attention_fp8_k_scale_per_query_head)]
+           ("attention_fp8_ref", _attention_fp8_k_scale_per_query_head),
+           ("verify_attention_fp8_ref", _verify_fp8_no_v_scale),
+           ("verify_attention_fp8_ref", _verify_fp8_k_scale_per_query_head),
+           ("verify_attention_fp8_ref", _verify_fp8_excludes_itself)]
 
 
 @pytest.mark.parametrize("name,mutant", MUTANTS, ids=lambda x: getattr(x, "__name__", x))
