@@ -41,6 +41,53 @@ def test_header_constants_match_the_binding():
     assert pkv.PLANNED & pkv.INPUTS_READY == 0
 
 
+def _c_kind(decl):
+    """A C parameter or return type from the header, reduced to what ctypes must pass."""
+    decl = re.sub(r"\b(const|struct)\b", " ", decl)
+    if "*" in decl:
+        return "char_p" if re.fullmatch(r"\s*char\s*\*\s*", decl) else "ptr"
+    t = decl.split()[0] if decl.split() else "void"
+    return {"int": "int", "pkv_dtype": "int", "pkv_status": "int", "int32_t": "int", "unsigned": "uint",
+            "int64_t": "int64", "size_t": "size", "float": "float", "void": "void"}[t]
+
+
+def _ctypes_kind(t):
+    if t is None:
+        return "void"
+    if t is ctypes.c_char_p:
+        return "char_p"
+    if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    return {ctypes.c_int: "int", ctypes.c_int32: "int", ctypes.c_uint: "uint", ctypes.c_int64: "int64",
+            ctypes.c_size_t: "size", ctypes.c_float: "float"}[t]
+
+
+def header_prototypes():
+    """name -> (return kind, [parameter kinds]) for every PKV_API declaration."""
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    protos = {}
+    for m in re.finditer(r"PKV_API\s+([\w\s\*]+?)\b(pkv_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(3).split(",") if p.strip() and p.strip() != "void"]
+        # a parameter's type is the declaration without its name
+        kinds = [_c_kind(re.sub(r"\b\w+\s*$", "", p) if not p.rstrip().endswith("*") else p) for p in params]
+        protos[m.group(2)] = (_c_kind(m.group(1)), kinds)
+    return protos
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes declaration in the binding passes what the header's prototype takes:
+    the same number of parameters, each a pointer, an int, a 64-bit int, a size or a float
+    where the header says so, and the same return type."""
+    protos = header_prototypes()
+    assert sorted(protos) == declared_symbols()
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        got = [_ctypes_kind(t) for t in (fn.argtypes or [])]
+        assert got == params, f"{name}: binding passes {got}, header declares {params}"
+        assert _ctypes_kind(fn.restype) == ret, f"{name}: binding returns {fn.restype}, header {ret}"
+
+
 def test_every_declared_symbol_is_exported(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\sT\s(pkv_\w+)$", out, re.M))
