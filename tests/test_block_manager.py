@@ -105,6 +105,30 @@ def test_last_holder_of_a_shared_block_needs_no_free_block():
     assert cow.tolist() == [[1, 2], [1, 3]] and [tuple(p) for p in want[1]] == [(1, 2), (1, 3)]
 
 
+def test_oracle_manager_follows_the_same_pages():
+    """The oracle's reference manager pinned to the same worked behaviour directly, not only
+    through the differential test: ceil-sized FIFO allocation with freed blocks at the back
+    (P2 §2.3, P4 §3), and a fork's partly filled block copied by every writer but the last
+    holder (P1 §4.2.2, P2 §3.3)."""
+    eng = oracle.BlockEngineRef(300, 16)
+    assert eng.allocate(0, 50) and eng.tables[0] == [0, 1, 2, 3]
+    assert eng.allocate(1, 4096) and eng.tables[1] == list(range(4, 260))
+    assert eng.free(0)
+    assert eng.allocate(2, 40 * 16) and eng.tables[2] == list(range(260, 300)) and len(eng.free_list) == 4
+    assert eng.allocate(3, 1) and eng.tables[3] == [0]
+    eng = oracle.BlockEngineRef(16, 16)
+    eng.allocate(0, 40)
+    eng.fork(0, 1)
+    eng.fork(0, 2)
+    assert eng.ref[:3] == [3, 3, 3]
+    slots, cow = eng.append_slots([1, 2, 0])
+    assert cow == [(2, 3), (2, 4)] and slots == [3 * 16 + 8, 4 * 16 + 8, 2 * 16 + 8]
+    assert eng.ref[:5] == [3, 3, 1, 1, 1]
+    eng.free(0)
+    eng.free(1)
+    assert eng.ref[0] == 1 and eng.ref[2] == 0 and len(eng.free_list) == 16 - 5 + 2
+
+
 def test_fork_at_block_boundary_needs_no_copy():
     bm = pkv.BlockManager(8, 16)
     bm.allocate(0, 32)
