@@ -55,6 +55,36 @@ def test_structure(name):
         assert np.array_equal(t[0, :nbp - 1], t[1, :nbp - 1]) and t[0, nbp - 1] != t[1, nbp - 1]
 
 
+def test_lengths_and_shapes_follow_the_recipe():
+    """The configurations' shapes and length distributions as the recipe states them (the
+    workload table of the measurement section): a generator drift here would move every
+    benchmark number without any test of the kernels noticing."""
+    shape = lambda n: (W.SPECS[n].num_heads, W.SPECS[n].num_kv_heads, W.SPECS[n].head_dim, W.SPECS[n].block_size,
+                       W.SPECS[n].dtype)
+    wl = W.build(W.SPECS["tiny"], values="none")
+    assert wl.seq_lens.tolist() == [1, 17, 33, 50] and shape("tiny") == (4, 4, 64, 16, W.F16)
+    for name in ("llama3_8b", "llama3_8b_fp8"):
+        L = W.build(W.SPECS[name], values="none").seq_lens
+        assert len(L) == 64 and L.min() >= 512 and L.max() <= 4096 and shape(name) == (32, 8, 128, 16, W.BF16)
+        assert L.min() < 800 and L.max() > 3800 and 1900 < L.mean() < 2700     # U[512, 4096]: mean 2304
+    for name, bs in (("llama2_70b_mixed_bs16", 16), ("llama2_70b_mixed_bs32", 32)):
+        L = W.build(W.SPECS[name], values="none").seq_lens
+        assert len(L) == 128 and L.min() >= 32 and L.max() <= 8192 and shape(name) == (64, 8, 128, bs, W.F16)
+        # lognormal, median 500, sigma 1.2: the sample median of 128 lies within about 0.3 of ln 500
+        assert 370 < np.median(L) < 680 and np.std(np.log(L)) > 0.9
+    a = W.build(W.SPECS["llama2_70b_mixed_bs16"], values="none").seq_lens
+    b = W.build(W.SPECS["llama2_70b_mixed_bs32"], values="none").seq_lens
+    assert np.array_equal(a, b)                                              # same lengths at both block sizes
+    for name, prefix in (("cow_fork", 1024), ("cow_fork_partial", 1020)):
+        wl = W.build(W.SPECS[name], values="none")
+        assert wl.spec.num_seqs == 768 and shape(name) == (32, 8, 128, 8, W.F16)
+        sfx = wl.seq_lens - prefix
+        assert sfx.min() >= 0 and sfx.max() <= 512 and sfx.max() > 480 and 200 < sfx.mean() < 310
+    wl = W.build(W.SPECS["llama2_70b_step"], values="none")
+    assert wl.spec.num_layers == 80 and (wl.seq_lens == 4096).all() and len(wl.seq_lens) == 16
+    assert shape("llama2_70b_step") == (64, 8, 128, 16, W.BF16)
+
+
 def test_tiny_values_and_poison():
     wl = W.build(W.SPECS["tiny"])
     assert wl.num_blocks == 32 and wl.seq_lens.tolist() == [1, 17, 33, 50]
