@@ -184,6 +184,11 @@ def test_fused_and_verify_validation_rejects_before_launch(lib):
     assert verify_fp8(v_scale=null) == pkv.PKV_ERR_INVALID
     assert verify_fp8(sum_lens=-5) == pkv.PKV_ERR_INVALID
     assert verify_fp8(head_dim=64) == pkv.PKV_ERR_UNSUPPORTED         # E4M3 pools: head_dim 128
+    # a 128K-position batch at 64-position partitions (2048 per sequence, past the 512 the merge
+    # holds) is refused before any driver call, naming the way out
+    st = lib.pkv_paged_attention_decode(fake, fake, fake, fake, fake, 8192, fake, 2, 131072, 8, 2, 128, 16, 20000,
+                                        1.0, 0, fake, 1 << 30, 64, null)
+    assert st == pkv.PKV_ERR_UNSUPPORTED and b"use a larger partition_tokens" in lib.pkv_last_error()
 
 
 def test_workspace_formula(lib):
