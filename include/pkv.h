@@ -165,7 +165,10 @@ PKV_API int pkv_decode_plan_partition_tokens(const void* workspace, int num_seqs
  *                 positions per resident CTA, an E4M3 position counting
  *                 1.4 times, multiples of 512, at least
  *                 pkv_decode_partition_tokens); the output does not depend
- *                 on that order.
+ *                 on that order.  A sequence may span at most 512
+ *                 partitions at the host's size: a longer max_seq_len with
+ *                 a small explicit size returns PKV_ERR_UNSUPPORTED (raise
+ *                 partition_tokens); 0 always picks a size that fits.
  *   Shared prefixes: the plan compares the block-table rows of adjacent
  *   sequences whose first entries agree (forks of one prompt, P2 §3.3) and,
  *   with at most 4 query heads per KV head and 16-bit pools, serves up to

@@ -132,6 +132,7 @@ bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32; }
 
 constexpr int kChunk = 64;
 constexpr int kMaxPartition = 4096;
+constexpr int kMaxPartsPerSeq = 512;               // partitions of one sequence a decode call accepts
 
 // Partition size for a decode batch.  1024 positions (measured best on the
 // 8B- and 70B-shaped batches), grown while a sequence would need more than 512
@@ -139,17 +140,19 @@ constexpr int kMaxPartition = 4096;
 // fill fewer than three waves of CTAs, the size in [512, 1024] (multiple of
 // 64) whose last wave is fullest is taken instead (a uniform 16 x 4096 batch
 // at three CTAs per SM: 640).  Below one wave, halved down to 128 while the
-// batch gives fewer than two CTAs per SM.
+// batch gives fewer than two CTAs per SM.  No step takes a sequence past 512
+// partitions unless even 4096 positions do (a max_seq_len above 2M).
 int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_seq_len, int sms, int ctas_per_sm) {
+    auto parts = [&](int q) { return (static_cast<int64_t>(max_seq_len) + q - 1) / q; };
     int p = 1024;
-    while (p < kMaxPartition && (max_seq_len + p - 1) / p > 512) p <<= 1;
+    while (p < kMaxPartition && parts(p) > kMaxPartsPerSeq) p <<= 1;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads * head_groups;
     const int64_t slots = static_cast<int64_t>(sms > 0 ? sms : 152) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
-    auto waves = [&](int q) { return static_cast<double>(pairs * ((max_seq_len + q - 1) / q)) / slots; };
+    auto waves = [&](int q) { return static_cast<double>(pairs * parts(q)) / slots; };
     if (p == 1024 && waves(1024) >= 1.0 && waves(1024) < 3.0) {
         double best = -1.0;
         int best_p = 1024;
-        for (int q = 1024; q >= 512; q -= 64) {
+        for (int q = 1024; q >= 512 && parts(q) <= kMaxPartsPerSeq; q -= 64) {
             const double w = waves(q);
             const double fill = w / static_cast<double>(static_cast<int64_t>(w + 0.999999));
             if (fill > best + 1e-9) {
@@ -159,7 +162,7 @@ int choose_partition(int num_seqs, int num_kv_heads, int head_groups, int max_se
         }
         return best_p;
     }
-    while (p > 128 && pairs * ((max_seq_len + p - 1) / p) < 2LL * (sms > 0 ? sms : 152)) p >>= 1;
+    while (p > 128 && pairs * parts(p) < 2LL * (sms > 0 ? sms : 152) && parts(p >> 1) <= kMaxPartsPerSeq) p >>= 1;
     return p;
 }
 
@@ -337,9 +340,9 @@ pkv_status attention_call(void* out, const void* q, const void* key_cache, const
     const int dev = current_device();
     const int part = resolve_partition(num_seqs, rows, num_kv_heads, max_seq_len, partition_tokens, head_dim);
     const int64_t base_parts = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + part - 1) / part : 1;
-    if (base_parts > 512)
-        return fail(PKV_ERR_UNSUPPORTED, "%lld partitions per sequence (at most 512; use a larger partition_tokens)",
-                    static_cast<long long>(base_parts));
+    if (base_parts > kMaxPartsPerSeq)
+        return fail(PKV_ERR_UNSUPPORTED, "%lld partitions per sequence (at most %d; use a larger partition_tokens)",
+                    static_cast<long long>(base_parts), kMaxPartsPerSeq);
     const int64_t max_parts = partial_slots(max_seq_len, part, rows / num_kv_heads);
     const pkv::DecodeWorkspace lay =
         pkv::decode_workspace_layout(num_seqs, rows, num_kv_heads, head_dim, static_cast<int>(max_parts));

@@ -259,11 +259,14 @@ def test_host_partition_rule_properties(lib):
     takes 152 SMs and one resident CTA per SM."""
     for B in (0, 1, 4, 16, 64, 128, 768, 65535):
         for Hq, Hkv in ((4, 4), (32, 8), (64, 8), (8, 1)):
-            for L in (0, 1, 50, 1024, 4096, 8192, 100000, 2 ** 21):
+            for L in (0, 1, 50, 1024, 4096, 8192, 66000, 100000, 400000, 600000, 2 ** 21):
                 for d in (64, 128):
                     p = lib.pkv_decode_partition_tokens(B, Hq, Hkv, d, L)
                     assert p % 64 == 0 and 128 <= p <= 4096, (B, Hq, Hkv, L, d, p)
                     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, L, p) != ctypes.c_size_t(-1).value
+                    # the automatic size never asks for more partitions than the call accepts (one
+                    # sequence of 66000 positions over one KV head once got 128 positions: 516)
+                    assert -(-L // p) <= 512, (B, Hq, Hkv, L, d, p)
     assert lib.pkv_decode_partition_tokens(4, 6, 4, 128, 100) < 0        # heads not a multiple of KV heads
     assert lib.pkv_decode_partition_tokens(4, 8, 2, 96, 100) < 0         # head_dim not built
 

@@ -38,6 +38,10 @@ LONG = [
     # 64K + 13 positions (a ragged last block), GQA 8, fp16, block size 32
     dict(num_seqs=2, num_heads=64, num_kv_heads=8, head_dim=128, block_size=32, dtype=W.F16, seed=72,
          lens=("fixed", (65549, 4096)), pool=("headroom", 0.05)),
+    # one 66000-position sequence over a single KV head (8 query heads): the automatic size
+    # must keep it within the 512 partitions a call accepts
+    dict(num_seqs=1, num_heads=8, num_kv_heads=1, head_dim=128, block_size=16, dtype=W.F16, seed=76,
+         lens=("fixed", (66000,)), pool=("headroom", 0.05)),
 ]
 
 
